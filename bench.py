@@ -1,0 +1,395 @@
+"""Benchmark of batched row-wise TopK on B300: effective HBM GB/s and rows/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl ours|reference]
+
+A step is one ds_topk call over one batch of the workload (the whole hot path:
+load, NaN check, threshold, radix select, ordered output write). The timed
+region holds exactly K steps replayed from CUDA graphs, bracketed by a barrier
+and a device synchronize; each step reads a different resident copy of the
+input whenever one batch fits in L2, so every step streams its input from HBM.
+Rank 0 prints one JSON line. Under torchrun every rank runs the same workload
+on its own GPU (rows are independent: no collective on the data path), and the
+value is the bytes of all ranks over the slowest rank's time.
+
+The metric is the pages' own: effective memory bandwidth, (input bytes read +
+output bytes written) / time, because TopK does no floating-point math
+(github-research.aiutil.com, "deepseek-ai/DeepSelect", section 关键技术亮点).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "effective HBM GB/s and rows/s for batched TopK (bf16 indexer, fp32 sampler)"
+DEFAULT_WORKLOAD = "c2"
+L2_BYTES_FALLBACK = 126 * 1024 * 1024
+FALLBACK_HBM_GBS = 6400.0
+KERNEL_SOURCES = ["sampler_topk_selection_ds_b300/csrc/topk_kernel.cuh",
+                  "sampler_topk_selection_ds_b300/csrc/ds_topk.cu"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary
+    of this workload, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None, None
+    if d.get("kernel_hash") != kernel_hash():
+        return None, "stale (kernel changed since the ncu capture)"
+    return d.get("dram_bytes_per_launch"), d.get("note")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self, t_start: float, t_end: float):
+        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        busy = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def _dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def _barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(bytes_per_step: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job effective GB/s: bytes moved by all ranks over the slowest rank's time."""
+    return bytes_per_step * steps * world / max_seconds / 1e9
+
+
+def cpu_baseline(w: workloads.Workload, min_seconds: float):
+    """The oracle as it stands on the host cores, on a bounded sample of the
+    workload: whole rows of the batch, as many as take about `min_seconds`."""
+    import oracle
+    cores = oracle.cores()
+    rows = list(range(w.batch))
+    # bound the sample: at most 256 rows (c4 has 16384)
+    if len(rows) > 256:
+        rows = rows[:: max(1, len(rows) // 256)][:256]
+    x = workloads.generate_rows(w, rows)
+    oracle.topk(x, w.k, return_value=w.return_value)  # warm
+    t_per_call, reps = oracle.time_topk(x, w.k, return_value=w.return_value, nthreads=0,
+                                        min_seconds=min_seconds)
+    sub = w.scaled(len(rows))
+    gbs = (sub.bytes_in + sub.bytes_out) / t_per_call / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(rows)} of {w.batch} rows of {w.name}, {reps} repeats "
+                      f"({t_per_call * 1e3:.1f} ms per repeat, all {cores} host threads)",
+            "rows_per_s": round(len(rows) / t_per_call, 2)}
+
+
+def run_reference(args, w):
+    world, rank, local = _dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    cb = cpu_baseline(w, min_seconds=max(2.0, min(20.0, 0.5 * args.steps)))
+    value = cb["value"]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w, None),
+        "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "reference arm = the CPU oracle (plain sort per row), host cores only",
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w, copies):
+    cfg = {"workload": f"{w.name}: {w.description}", "batch": w.batch, "len": w.length, "k": w.k,
+           "input_dtype": "bf16" if w.dtype == torch.bfloat16 else "fp32",
+           "sorted_index": w.sorted_index, "return_value": w.return_value,
+           "seed": w.seed, "parallelism": "rows independent; one GPU per rank (weak scaling)"}
+    if copies is not None:
+        cfg["l2"] = copies
+    return cfg
+
+
+def run_ours(args, w):
+    import sampler_topk_selection_ds_b300 as dstk
+
+    world, rank, local = _dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK
+
+    # resident inputs: enough copies that one step's input is cold in L2
+    copies = 1 if w.bytes_in >= 4 * l2 else min(64, math.ceil(4 * l2 / w.bytes_in))
+    x0 = workloads.generate(w, device=dev)
+    xs = [x0] + [x0.clone() for _ in range(copies - 1)]
+    l2_note = (f"inputs larger than L2 ({w.bytes_in / 1e6:.0f} MB per step > {l2 / 1e6:.0f} MB)"
+               if copies == 1 else
+               f"rotating {copies} resident input copies ({copies * w.bytes_in / 1e6:.0f} MB > 4x L2 "
+               f"{l2 / 1e6:.0f} MB); each step reads a copy not touched for {copies - 1} steps")
+    dt_code = dstk.dtype_code(w.dtype)
+    idx = torch.empty((w.batch, w.k), dtype=torch.int32, device=dev)
+    vals = torch.empty((w.batch, w.k), dtype=w.dtype, device=dev) if w.return_value else None
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    rc, plan = dstk.ds_topk_plan(dt_code, w.batch, w.length, w.length, w.k, props.multi_processor_count)
+    assert rc == dstk.OK, dstk.status_string(rc)
+
+    def step(i, stream):
+        r = dstk.ds_topk(xs[i % copies].data_ptr(), dt_code, w.batch, w.length, w.length, w.k,
+                         int(w.sorted_index), int(w.return_value),
+                         vals.data_ptr() if vals is not None else None, idx.data_ptr(),
+                         flag.data_ptr(), stream.cuda_stream)
+        if r != dstk.OK:
+            raise dstk.DsTopkError(r)
+
+    stream = torch.cuda.Stream(dev)
+    warmup = max(3, args.warmup)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i, stream)
+    stream.synchronize()
+
+    # CUDA graphs of `chunk` steps (a multiple of the rotation) + a remainder graph
+    chunk = copies * max(1, math.ceil(64 / copies))
+    full, rem = divmod(args.steps, chunk)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i, torch.cuda.current_stream())
+        return g
+
+    g_full = capture(chunk) if full else None
+    g_rem = capture(rem) if rem else None
+    if g_full is not None:
+        g_full.replay()
+    stream.synchronize()
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    with sampler:
+        _barrier(world)
+        torch.cuda.synchronize(dev)
+        t_wall0 = time.time()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(full):
+                g_full.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            ev1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize(dev)
+        _barrier(world)
+        t_wall1 = time.time()
+    seconds = ev0.elapsed_time(ev1) / 1e3
+    max_seconds = _max_over_ranks(seconds, world)
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    bytes_step = w.bytes_in + w.bytes_out
+    value = aggregate_value(bytes_step, args.steps, world, max_seconds)
+    per_launch_s = seconds / (args.steps * plan.launches)
+    achieved = bytes_step / plan.launches / per_launch_s / 1e9
+    peak, peak_src = measured_peak()
+    traffic, traffic_note = profiled_traffic(w.name)
+
+    # end to end through the public API with host buffers (pinned), copies inside
+    e2e = e2e_measure(w, dstk, dev, stream, min(args.steps, args.e2e_steps))
+    cb = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(w, min_seconds=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": warmup,
+            "ms_per_step": round(max_seconds / args.steps * 1e3, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "u16" if w.dtype == torch.bfloat16 else "u32",
+            "data": "synthetic (seeded SplitMix64 + Box-Muller, workloads.py)",
+            "config": _config(w, l2_note),
+            "rows_per_s": round(w.batch * args.steps * world / max_seconds, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_source": peak_src + (" (of measured)" if peak_src != "fallback" else " (of fallback)"),
+                         "traffic": traffic, "traffic_note": traffic_note,
+                         "kernel": f"topk_rows_kernel<{2 if w.dtype == torch.bfloat16 else 4},{plan.cluster_size}>",
+                         "kernel_hash": kernel_hash()},
+            "e2e": e2e,
+            "gpu_launches": args.steps * plan.launches,
+            "plan": plan.as_dict(),
+            "clocks": clocks,
+            "cpu_baseline": cb,
+            "gpu": props.name,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_measure(w, dstk, dev, stream, steps):
+    """Same metric through topk() with the input in pinned host memory: every step
+    copies the batch host->device, selects, and copies the outputs back."""
+    steps = max(1, steps)
+    x_host = workloads.generate(w).pin_memory()
+    x_dev = torch.empty_like(x_host, device=dev)
+    idx_dev = torch.empty((w.batch, w.k), dtype=torch.int32, device=dev)
+    vals_dev = torch.empty((w.batch, w.k), dtype=w.dtype, device=dev) if w.return_value else None
+    idx_host = torch.empty((w.batch, w.k), dtype=torch.int32).pin_memory()
+    vals_host = torch.empty((w.batch, w.k), dtype=w.dtype).pin_memory() if w.return_value else None
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def one():
+        x_dev.copy_(x_host, non_blocking=True)
+        dstk.topk(x_dev, w.k, sorted_index=w.sorted_index, return_value=w.return_value,
+                  nan_flag=flag, out=(vals_dev, idx_dev), stream=stream)
+        idx_host.copy_(idx_dev, non_blocking=True)
+        if vals_host is not None:
+            vals_host.copy_(vals_dev, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+    stream.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3
+    h2d = w.bytes_in
+    d2h = w.batch * w.k * 4 + (w.batch * w.k * w.elem_size if w.return_value else 0)
+    return {"value": round((w.bytes_in + w.bytes_out) * steps / sec / 1e9, 3), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(sec / steps * 1e3, 4)}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

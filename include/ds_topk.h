@@ -31,6 +31,13 @@
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define DS_TOPK_API __attribute__((visibility("default")))
+#else
+#define DS_TOPK_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -112,7 +119,7 @@ typedef enum {
  * shared mutable state besides a per-device cache of launch attributes that is
  * filled under a lock).
  */
-int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
+DS_TOPK_API int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
             int k, int sorted_index, int return_value, void* out_values,
             int32_t* out_indices, int32_t* nan_flag, cudaStream_t stream);
 
@@ -128,7 +135,9 @@ typedef struct {
   int32_t cluster_size;        /* CTAs cooperating on one row (1 for DS_TOPK_PATH_ROW) */
   int32_t threads_per_cta;
   int32_t vectors_per_granule; /* 16-byte vectors summarised by one granule maximum     */
-  int64_t grid_ctas;           /* CTAs launched                                        */
+  int64_t grid_ctas;           /* CTAs if every row had its own cluster; ds_topk launches
+                                  at most as many as can be co-resident, and each
+                                  persistent cluster then walks rows with a stride      */
   int64_t granules_per_cta;    /* size of the per-CTA granule-maximum array            */
   int32_t smem_bytes;          /* dynamic shared memory per CTA                        */
   int32_t launches;            /* kernel launches per call                             */
@@ -141,14 +150,14 @@ typedef struct {
  * (x/output pointers are not involved). Returns DS_TOPK_OK or DS_TOPK_EINVAL /
  * DS_TOPK_EALIGN; plan must be non-NULL and sm_count >= 1.
  */
-int ds_topk_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k,
+DS_TOPK_API int ds_topk_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k,
                  int sm_count, ds_topk_plan_t* plan);
 
 /* Short static description of a status code ("ok", "invalid argument", ...). */
-const char* ds_topk_status_string(int status);
+DS_TOPK_API const char* ds_topk_status_string(int status);
 
 /* Library version, e.g. 100 for 0.1.0. */
-int ds_topk_version(void);
+DS_TOPK_API int ds_topk_version(void);
 
 #ifdef __cplusplus
 }

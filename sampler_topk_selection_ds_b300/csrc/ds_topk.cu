@@ -1,0 +1,356 @@
+// ds_topk.cu — host side of libds_topk.so: argument validation, launch planning
+// and kernel launches behind the C ABI declared in include/ds_topk.h.
+//
+// The call surface restates deep_select.topk(x, topk, sorted_index, indices_type)
+// and its return_value option (deepseek.csdn.net, "DeepSeek 一次开源三个仓库",
+// section 三; deepseek-v4-pro.uk (zh-tw), section "DeepSelect：快速且刻意狹義的
+// TopK") as one C function over raw device pointers. The pages say the fastest
+// algorithm depends on dtype, batch, row length and k (github-research.aiutil.com,
+// "deepseek-ai/DeepSelect", section 关键技术亮点); the plan below picks how many
+// CTAs share one row from those sizes and the SM count.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "ds_topk.h"
+#include "topk_kernel.cuh"
+
+namespace {
+
+using ds_topk_dev::kGranuleCap;
+using ds_topk_dev::kMiscWords;
+using ds_topk_dev::kRadix;
+using ds_topk_dev::kThreads;
+using ds_topk_dev::Params;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxCluster = 16;
+// Rows at most this long (bytes) are never split: one CTA streams them.
+constexpr int64_t kSplitMinRowBytes = 64 * 1024;
+// A CTA of a split row gets at least this many bytes of it.
+constexpr int64_t kMinSliceBytes = 16 * 1024;
+// Bounds of the per-CTA shared-memory copy of the listed granules (16-byte vectors).
+constexpr int64_t kCacheMinVecs = 512;
+constexpr int64_t kCacheMaxVecs = 4096;
+
+struct Plan {
+  ds_topk_plan_t pub;
+  Params prm;
+  int es;
+};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int validate_sizes(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k) {
+  if (dtype != DS_TOPK_BF16 && dtype != DS_TOPK_FP32) return DS_TOPK_EINVAL;
+  if (batch < 0 || len < 1 || len > INT32_MAX || row_stride < len) return DS_TOPK_EINVAL;
+  if (k < 1 || k > DS_TOPK_MAX_K || static_cast<int64_t>(k) > len) return DS_TOPK_EINVAL;
+  const int64_t es = dtype == DS_TOPK_BF16 ? 2 : 4;
+  if (row_stride > INT64_MAX / es) return DS_TOPK_EINVAL;
+  if (batch > 0 && row_stride * es > INT64_MAX / batch) return DS_TOPK_EINVAL;
+  if ((row_stride * es) % 16 != 0) return DS_TOPK_EALIGN;
+  return DS_TOPK_OK;
+}
+
+// Pure host planning: how the rows map onto CTAs and clusters.
+int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, int sm_count,
+              int max_cluster, Plan* out) {
+  const int rc = validate_sizes(dtype, batch, len, row_stride, k);
+  if (rc != DS_TOPK_OK) return rc;
+  if (sm_count < 1) return DS_TOPK_EINVAL;
+  const int es = dtype == DS_TOPK_BF16 ? 2 : 4;
+  const int vec = 16 / es;
+  const int64_t nvec = ceil_div(len, vec);
+  const int64_t row_bytes = len * es;
+
+  int S = 1;
+  if (row_bytes > kSplitMinRowBytes && batch < 2 * static_cast<int64_t>(sm_count)) {
+    const int64_t want = ceil_div(2 * static_cast<int64_t>(sm_count), batch > 0 ? batch : 1);
+    const int64_t by_size = row_bytes / kMinSliceBytes;
+    while (S < max_cluster && S * 2 <= want && S * 2 <= by_size) S *= 2;
+    if (S < 2 && by_size >= 2 && want >= 2) S = 2;
+    if (S > max_cluster) S = max_cluster;
+  }
+  const int64_t vec_per_cta = ceil_div(nvec, S);
+  const int64_t gv = ceil_div(vec_per_cta, kGranuleCap);
+  const int64_t g_cap = ceil_div(vec_per_cta, gv);
+  const int64_t g_cap_pad = (g_cap + 7) & ~int64_t(7);
+  int64_t g_total = 0;
+  for (int r = 0; r < S; ++r) {
+    int64_t n = nvec - r * vec_per_cta;
+    if (n > vec_per_cta) n = vec_per_cta;
+    if (n > 0) g_total += ceil_div(n, gv);
+  }
+  const int64_t grid = batch * S;
+  if (grid > INT32_MAX) return DS_TOPK_EINVAL;
+  // Shared-memory copy of the granules that pass the threshold: about k of them
+  // for data without heavy ties; more (ties, sorted rows) fall back to L2 reads.
+  int64_t cache_vecs = 2 * static_cast<int64_t>(k);
+  if (cache_vecs < kCacheMinVecs) cache_vecs = kCacheMinVecs;
+  if (cache_vecs > kCacheMaxVecs) cache_vecs = kCacheMaxVecs;
+  if (cache_vecs > vec_per_cta) cache_vecs = vec_per_cta;
+  // Dense candidate array: typically about k entries (one per listed granule).
+  int64_t cand_cap = 2 * cache_vecs;
+  if (cand_cap > vec_per_cta * vec) cand_cap = vec_per_cta * vec;
+  const int64_t smem = ds_topk_dev::smem_bytes(g_cap_pad, cache_vecs, cand_cap);
+
+  out->es = es;
+  ds_topk_plan_t& pl = out->pub;
+  pl.path = S > 1 ? DS_TOPK_PATH_CLUSTER : DS_TOPK_PATH_ROW;
+  pl.cluster_size = S;
+  pl.threads_per_cta = kThreads;
+  pl.vectors_per_granule = static_cast<int32_t>(gv);
+  pl.grid_ctas = grid;
+  pl.granules_per_cta = g_cap;
+  pl.smem_bytes = static_cast<int32_t>(smem);
+  pl.launches = batch > 0 ? 1 : 0;
+
+  Params& p = out->prm;
+  p.x = nullptr;
+  p.batch = batch;
+  p.row_stride_bytes = row_stride * es;
+  p.len = len;
+  p.nvec = nvec;
+  p.vec_per_cta = vec_per_cta;
+  p.g_total = g_total;
+  p.gv = static_cast<int32_t>(gv);
+  p.g_cap_pad = static_cast<int32_t>(g_cap_pad);
+  p.cache_vecs = static_cast<int32_t>(cache_vecs);
+  p.cand_cap = static_cast<int32_t>(cand_cap);
+  p.k = k;
+  p.return_value = 0;
+  p.out_values = nullptr;
+  p.out_indices = nullptr;
+  p.flag = nullptr;
+  return DS_TOPK_OK;
+}
+
+// Per-device facts, filled once under a lock.
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  int max_cluster = 8;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+constexpr int kMaxSmem =
+    static_cast<int>(ds_topk_dev::smem_bytes(kGranuleCap, kCacheMaxVecs, 2 * kCacheMaxVecs));
+static_assert(kMaxSmem <= 227 * 1024, "shared memory per CTA");
+
+template <int ES, int S>
+cudaError_t prepare_kernel() {
+  auto* fn = ds_topk_dev::topk_rows_kernel<ES, S>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+  if (e != cudaSuccess) return e;
+  if (S > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+template <int ES>
+cudaError_t prepare_dtype() {
+  cudaError_t e;
+  if ((e = prepare_kernel<ES, 1>()) != cudaSuccess) return e;
+  if ((e = prepare_kernel<ES, 2>()) != cudaSuccess) return e;
+  if ((e = prepare_kernel<ES, 4>()) != cudaSuccess) return e;
+  if ((e = prepare_kernel<ES, 8>()) != cudaSuccess) return e;
+  return prepare_kernel<ES, 16>();
+}
+
+// Largest cluster size (<= 16) that can be resident with the biggest CTA we launch.
+template <int ES>
+int probe_cluster16() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(16, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kMaxSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 16;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, ds_topk_dev::topk_rows_kernel<ES, 16>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DS_TOPK_ECUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+      return DS_TOPK_ECUDA;
+    if (prepare_dtype<2>() != cudaSuccess || prepare_dtype<4>() != cudaSuccess) return DS_TOPK_ECUDA;
+    const int c16 = (probe_cluster16<2>() > 0 && probe_cluster16<4>() > 0) ? 16 : 8;
+    d.sm_count = sms;
+    d.max_cluster = c16;
+    d.ready = true;
+  }
+  *out = d;
+  return DS_TOPK_OK;
+}
+
+// How many clusters of S CTAs (S = 1: plain CTAs) of this kernel can be resident
+// at once with `smem` bytes of dynamic shared memory each.
+template <int ES, int S>
+int resident_clusters(int smem, int sm_count) {
+  auto* fn = ds_topk_dev::topk_rows_kernel<ES, S>;
+  int n = 0;
+  if (S == 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return n * sm_count;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+struct ResidencyEntry {
+  int dev, es, S, smem, clusters;
+};
+constexpr int kResidencySlots = 64;
+ResidencyEntry g_residency[kResidencySlots];
+int g_residency_used = 0;
+
+// Cached resident_clusters() per (device, dtype, cluster size, shared memory).
+int resident_cached(int dev, int es, int S, int smem, int sm_count) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int i = 0; i < g_residency_used; ++i) {
+    const ResidencyEntry& e = g_residency[i];
+    if (e.dev == dev && e.es == es && e.S == S && e.smem == smem) return e.clusters;
+  }
+  int n = 0;
+  switch (S) {
+    case 1: n = es == 2 ? resident_clusters<2, 1>(smem, sm_count) : resident_clusters<4, 1>(smem, sm_count); break;
+    case 2: n = es == 2 ? resident_clusters<2, 2>(smem, sm_count) : resident_clusters<4, 2>(smem, sm_count); break;
+    case 4: n = es == 2 ? resident_clusters<2, 4>(smem, sm_count) : resident_clusters<4, 4>(smem, sm_count); break;
+    case 8: n = es == 2 ? resident_clusters<2, 8>(smem, sm_count) : resident_clusters<4, 8>(smem, sm_count); break;
+    default: n = es == 2 ? resident_clusters<2, 16>(smem, sm_count) : resident_clusters<4, 16>(smem, sm_count); break;
+  }
+  if (g_residency_used < kResidencySlots) g_residency[g_residency_used++] = {dev, es, S, smem, n};
+  return n;
+}
+
+template <int ES, int S>
+cudaError_t launch_one(const Plan& pl, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.pub.grid_ctas), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(pl.pub.smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (S > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, ds_topk_dev::topk_rows_kernel<ES, S>, pl.prm);
+}
+
+template <int ES>
+cudaError_t launch_dtype(const Plan& pl, cudaStream_t stream) {
+  switch (pl.pub.cluster_size) {
+    case 1: return launch_one<ES, 1>(pl, stream);
+    case 2: return launch_one<ES, 2>(pl, stream);
+    case 4: return launch_one<ES, 4>(pl, stream);
+    case 8: return launch_one<ES, 8>(pl, stream);
+    case 16: return launch_one<ES, 16>(pl, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+}  // namespace
+
+extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
+                       int k, int sorted_index, int return_value, void* out_values,
+                       int32_t* out_indices, int32_t* nan_flag, cudaStream_t stream) {
+  int rc = validate_sizes(dtype, batch, len, row_stride, k);
+  if (rc != DS_TOPK_OK) return rc;
+  if ((sorted_index != 0 && sorted_index != 1) || (return_value != 0 && return_value != 1))
+    return DS_TOPK_EINVAL;
+  if (batch == 0) return DS_TOPK_OK;
+  if (!x || !out_indices || !nan_flag || (return_value && !out_values)) return DS_TOPK_EINVAL;
+  const int es = dtype == DS_TOPK_BF16 ? 2 : 4;
+  if (misaligned(x, 16) || misaligned(out_indices, 4) || misaligned(nan_flag, 4) ||
+      (return_value && misaligned(out_values, es)))
+    return DS_TOPK_EALIGN;
+
+  DeviceInfo dev;
+  rc = device_info(&dev);
+  if (rc != DS_TOPK_OK) return rc;
+  Plan pl;
+  rc = make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, &pl);
+  if (rc != DS_TOPK_OK) return rc;
+  pl.prm.x = static_cast<const char*>(x);
+  pl.prm.return_value = return_value;
+  pl.prm.out_values = return_value ? out_values : nullptr;
+  pl.prm.out_indices = out_indices;
+  pl.prm.flag = nan_flag;
+  // Persistent launch: no more clusters than can be resident at once; each one
+  // walks the rows with a stride (and reuses its threshold from row to row).
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  const int resident = resident_cached(dev_id, pl.es, pl.pub.cluster_size, pl.pub.smem_bytes,
+                                       dev.sm_count);
+  if (resident > 0 && batch > resident) pl.pub.grid_ctas = static_cast<int64_t>(resident) * pl.pub.cluster_size;
+
+  const cudaError_t e = es == 2 ? launch_dtype<2>(pl, stream) : launch_dtype<4>(pl, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return DS_TOPK_ECUDA;
+  }
+  if (cudaGetLastError() != cudaSuccess) return DS_TOPK_ECUDA;
+  return DS_TOPK_OK;
+}
+
+extern "C" int ds_topk_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k,
+                            int sm_count, ds_topk_plan_t* plan) {
+  if (!plan) return DS_TOPK_EINVAL;
+  Plan pl;
+  const int rc = make_plan(dtype, batch, len, row_stride, k, sm_count, kMaxCluster, &pl);
+  if (rc == DS_TOPK_OK) *plan = pl.pub;
+  return rc;
+}
+
+extern "C" const char* ds_topk_status_string(int status) {
+  switch (status) {
+    case DS_TOPK_OK: return "ok";
+    case DS_TOPK_EINVAL: return "invalid argument";
+    case DS_TOPK_EALIGN: return "misaligned pointer or row stride";
+    case DS_TOPK_ECUDA: return "CUDA runtime error";
+    case DS_TOPK_ETIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int ds_topk_version(void) { return 100; }

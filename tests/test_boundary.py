@@ -1,0 +1,103 @@
+"""The C-ABI boundary on the CPU: the library loads, exports every symbol the
+header declares, rejects bad arguments with the documented code before touching
+the GPU, and plans launches as documented. No call here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sampler_topk_selection_ds_b300 as dstk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            text = open(os.path.join(inc, fn), encoding="utf-8").read()
+            names |= set(re.findall(r"DS_TOPK_API\s+[\w\s\*]*?\b(ds_topk\w*)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared_symbols()
+    assert {"ds_topk", "ds_topk_plan", "ds_topk_status_string", "ds_topk_version"} <= names
+    lib = ctypes.CDLL(dstk.LIB_PATH)
+    for n in sorted(names):
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_version_and_status_strings():
+    assert dstk.version() >= 100
+    assert dstk.status_string(dstk.OK) == "ok"
+    assert "invalid" in dstk.status_string(dstk.EINVAL)
+    assert "align" in dstk.status_string(dstk.EALIGN)
+    assert dstk.status_string(99) == "unknown status"
+
+
+# Pointers below are never dereferenced: every call fails validation first.
+P = 1 << 20  # a 16-byte-aligned fake address
+
+
+@pytest.mark.parametrize("args,code", [
+    # (x, dtype, batch, len, row_stride, k, sorted, retval, out_values, out_indices, flag)
+    ((P, 2, 1, 16, 16, 1, 0, 1, P, P, P), dstk.EINVAL),          # bad dtype
+    ((P, 0, -1, 16, 16, 1, 0, 1, P, P, P), dstk.EINVAL),         # negative batch
+    ((P, 0, 1, 0, 16, 1, 0, 1, P, P, P), dstk.EINVAL),           # len 0
+    ((P, 0, 1, 2**31, 2**31, 1, 0, 1, P, P, P), dstk.EINVAL),    # len > INT32_MAX
+    ((P, 0, 1, 16, 8, 1, 0, 1, P, P, P), dstk.EINVAL),           # row_stride < len
+    ((P, 0, 1, 16, 16, 0, 0, 1, P, P, P), dstk.EINVAL),          # k = 0
+    ((P, 0, 1, 8192, 8192, 4097, 0, 1, P, P, P), dstk.EINVAL),   # k > 4096
+    ((P, 0, 1, 16, 16, 17, 0, 1, P, P, P), dstk.EINVAL),         # k > len
+    ((P, 0, 1, 16, 16, 1, 2, 1, P, P, P), dstk.EINVAL),          # sorted_index not 0/1
+    ((P, 0, 1, 16, 16, 1, 0, 3, P, P, P), dstk.EINVAL),          # return_value not 0/1
+    ((0, 0, 1, 16, 16, 1, 0, 1, P, P, P), dstk.EINVAL),          # x NULL
+    ((P, 0, 1, 16, 16, 1, 0, 1, P, 0, P), dstk.EINVAL),          # out_indices NULL
+    ((P, 0, 1, 16, 16, 1, 0, 1, P, P, 0), dstk.EINVAL),          # nan_flag NULL
+    ((P, 0, 1, 16, 16, 1, 0, 1, 0, P, P), dstk.EINVAL),          # values requested, NULL
+    ((P + 8, 0, 1, 16, 16, 1, 0, 1, P, P, P), dstk.EALIGN),      # x not 16-byte aligned
+    ((P, 0, 2, 12, 12, 1, 0, 1, P, P, P), dstk.EALIGN),          # bf16 stride 24 bytes
+    ((P, 1, 2, 6, 6, 1, 0, 1, P, P, P), dstk.EALIGN),            # fp32 stride 24 bytes
+    ((P, 0, 1, 16, 16, 1, 0, 1, P, P + 2, P), dstk.EALIGN),      # out_indices misaligned
+    ((P, 0, 1, 16, 16, 1, 0, 1, P, P, P + 1), dstk.EALIGN),      # flag misaligned
+    ((P, 1, 1, 16, 16, 1, 0, 1, P + 2, P, P), dstk.EALIGN),      # fp32 values misaligned
+    ((P, 0, 2**40, 2**30, 2**30, 1, 0, 1, P, P, P), dstk.EINVAL),  # batch*stride overflows
+])
+def test_argument_errors(args, code):
+    assert dstk.ds_topk(*args, 0) == code
+
+
+def test_batch_zero_is_ok_without_pointers():
+    assert dstk.ds_topk(0, dstk.BF16, 0, 100, 128, 5, 0, 0, None, 0, 0, 0) == dstk.OK
+
+
+def test_plan_shapes():
+    rc, p = dstk.ds_topk_plan(dstk.BF16, 16384, 32768, 32768, 512, 148)
+    assert rc == 0 and p.path == dstk.PATH_ROW and p.cluster_size == 1
+    assert p.grid_ctas == 16384 and p.vectors_per_granule == 1 and p.launches == 1
+    rc, p = dstk.ds_topk_plan(dstk.FP32, 64, 129280, 129280, 512, 148)
+    assert rc == 0 and p.path == dstk.PATH_CLUSTER and p.cluster_size in (2, 4, 8, 16)
+    assert p.grid_ctas == 64 * p.cluster_size
+    rc, p = dstk.ds_topk_plan(dstk.BF16, 8, 1 << 20, 1 << 20, 4096, 148)
+    assert rc == 0 and p.cluster_size == 16 and p.granules_per_cta <= 8192
+    rc, p = dstk.ds_topk_plan(dstk.FP32, 1, (1 << 23) + 3, (1 << 23) + 4, 4096, 148)
+    assert rc == 0 and p.cluster_size == 16 and p.vectors_per_granule > 1
+    assert p.granules_per_cta <= 8192
+    rc, p = dstk.ds_topk_plan(dstk.FP32, 0, 100, 100, 5, 148)
+    assert rc == 0 and p.launches == 0
+    # small rows are never split
+    rc, p = dstk.ds_topk_plan(dstk.FP32, 4, 4096, 4096, 64, 148)
+    assert rc == 0 and p.cluster_size == 1
+    # validation is shared with ds_topk
+    assert dstk.ds_topk_plan(dstk.FP32, 1, 10, 10, 11, 148)[0] == dstk.EINVAL
+    assert dstk.ds_topk_plan(dstk.FP32, 1, 10, 12, 5, 0)[0] == dstk.EINVAL
+    assert dstk.ds_topk_plan(dstk.BF16, 2, 10, 10, 5, 148)[0] == dstk.EALIGN
+
+
+def test_binding_has_no_cpu_fallback():
+    import torch
+    with pytest.raises(ValueError):
+        dstk.topk(torch.zeros(2, 16), 3)

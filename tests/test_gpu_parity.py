@@ -1,0 +1,233 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, bit-exact.
+
+Indices and values must equal the oracle's exactly (selection does no
+arithmetic). With sorted_index=0 the order is unspecified by contract, so both
+sides are compared after sorting by index; with sorted_index=1 the GPU order
+itself must be ascending. Rows holding a NaN are only checked for the flag and
+for in-range outputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._util import bits_of, check_invariants
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test run without a CUDA device")
+    torch.cuda.init()
+    yield
+
+
+def _dstk():
+    import sampler_topk_selection_ds_b300 as dstk
+    return dstk
+
+
+def _aligned(x, length):
+    """Rows whose byte length is not a multiple of 16 are copied into a padded
+    buffer (NaN padding, which must never be read)."""
+    es = x.element_size()
+    if x.stride(0) * es % 16 == 0 or x.shape[0] == 1:
+        return x, length
+    stride = -(-x.shape[1] * es // 16) * 16 // es
+    xp = torch.full((x.shape[0], stride), float("nan"), dtype=x.dtype, device=x.device)
+    xp[:, :x.shape[1]] = x
+    return xp, x.shape[1] if length is None else length
+
+
+def run_gpu(x, k, sorted_index, return_value, length=None, stream=None):
+    dstk = _dstk()
+    x, length = _aligned(x, length)
+    xd = x if x.is_cuda else x.cuda()
+    flag = torch.zeros(1, dtype=torch.int32, device=xd.device)
+    vals, idx = dstk.topk(xd, k, sorted_index=sorted_index, return_value=return_value,
+                          length=length, nan_flag=flag, stream=stream)
+    torch.cuda.synchronize()
+    return (vals.cpu() if vals is not None else None), idx.cpu(), int(flag.item())
+
+
+def assert_parity(x_cpu, k, sorted_index=False, return_value=True, length=None, rows=None,
+                  gpu_out=None):
+    """Compare GPU output with the oracle on rows `rows` (all rows by default)."""
+    length = x_cpu.shape[1] if length is None else length
+    if gpu_out is None:
+        gv, gi, gf = run_gpu(x_cpu, k, sorted_index, return_value, length)
+    else:
+        gv, gi, gf = gpu_out
+    sel = list(range(x_cpu.shape[0])) if rows is None else list(rows)
+    ov, oi, of, row_nan = oracle.topk(x_cpu[sel].contiguous(), k, length=length, return_value=True)
+    if rows is None:
+        assert gf == of, f"nan flag gpu={gf} oracle={of}"
+    for j, b in enumerate(sel):
+        g_idx = gi[b].numpy().astype(np.int64)
+        assert g_idx.min() >= 0 and g_idx.max() < length
+        if row_nan[j]:
+            continue
+        if sorted_index:
+            assert np.all(np.diff(g_idx) > 0), f"row {b}: sorted_index output not ascending"
+            order = np.arange(k)
+        else:
+            order = np.argsort(g_idx, kind="stable")
+        o_idx = oi[j].numpy().astype(np.int64)
+        if not np.array_equal(g_idx[order], o_idx):
+            bad = np.nonzero(g_idx[order] != o_idx)[0]
+            raise AssertionError(f"row {b}: {bad.size} index mismatches, first at {bad[0]}: "
+                                 f"gpu {g_idx[order][bad[0]]} oracle {o_idx[bad[0]]}")
+        if return_value:
+            assert np.array_equal(bits_of(gv[b])[order], bits_of(ov[j])), f"row {b}: values differ"
+
+
+# ---- the five workloads at full size ---------------------------------------------------
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c5"])
+def test_workload_full_parity(name):
+    w = workloads.WORKLOADS[name]
+    x = workloads.generate(w)
+    assert_parity(x, w.k, w.sorted_index, w.return_value)
+
+
+def test_workload_c4_full_sampled():
+    """c4 (16384 x 32768 bf16): the whole batch on the GPU in the benchmark's launch
+    configuration, the oracle on 48 sampled rows, properties on every row."""
+    w = workloads.WORKLOADS["c4"]
+    xd = workloads.generate(w, device="cuda")
+    gv, gi, gf = run_gpu(xd, w.k, w.sorted_index, w.return_value)
+    assert gv is None and gf == 0
+    rows = sorted(set([0, 1, 2, w.batch - 1] + list(range(7, w.batch, w.batch // 44))))
+    x_rows = xd[rows].cpu()
+    sub = (None, gi[rows], gf)
+    assert_parity(x_rows, w.k, w.sorted_index, w.return_value, gpu_out=sub)
+    # every row: in range, unique, never from the -inf tail (k <= #finite)
+    gi64 = gi.to(torch.int64)
+    s = torch.sort(gi64, dim=1).values
+    assert (s[:, 1:] > s[:, :-1]).all()
+    assert s.min().item() >= 0 and s.max().item() < 24576
+
+
+# ---- sweeps ------------------------------------------------------------------------------
+
+SWEEP = [
+    # (length, batch, k list)
+    (1, 3, [1]),
+    (7, 3, [1, 2, 7]),
+    (31, 5, [1, 2, 31]),
+    (4096, 3, [1, 2, 64, 512, 1024, 4095, 4096]),
+    (4097, 3, [1, 64, 4096]),
+    (65541, 3, [1, 512, 4096]),
+    (129280, 3, [64, 512, 4096]),
+    (204800, 2, [1024, 4096]),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("length,batch,ks", SWEEP)
+def test_sweep_normal(dtype, length, batch, ks):
+    x = workloads.random_rows(batch, length, dtype, 1000 + length, style="normal")
+    for k in ks:
+        assert_parity(x, k, sorted_index=(k % 2 == 0), return_value=True)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("style", ["ties", "allequal", "signed_zero", "denormal", "ramp"])
+@pytest.mark.parametrize("length", [33, 4096, 70001])
+def test_sweep_adversarial_styles(dtype, style, length):
+    x = workloads.random_rows(3, length, dtype, 77, style=style)
+    for k in sorted({1, min(64, length), min(4096, length), min(length, 4096)}):
+        assert_parity(x, k, sorted_index=True, return_value=True)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_row_stride_padding_and_tail(dtype):
+    # len not a multiple of the 16-byte vector, padding filled with NaN (never read)
+    for length, stride in [(5, 8), (1001, 1024), (65537, 65600)]:
+        es = 2 if dtype == torch.bfloat16 else 4
+        stride = -(-stride * es // 16) * 16 // es
+        x = workloads.random_rows(4, length, dtype, 5, style="normal", row_stride=stride)
+        k = min(100, length)
+        gv, gi, gf = run_gpu(x, k, True, True, length=length)
+        assert gf == 0
+        assert_parity(x, k, True, True, length=length, gpu_out=(gv, gi, gf))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_batch_many_short_rows(dtype):
+    x = workloads.random_rows(3000, 1000, dtype, 11, style="ties")
+    assert_parity(x, 37, sorted_index=False, return_value=True)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_long_single_row_coarse_granules(dtype):
+    """A row long enough that each cluster CTA summarises several vectors per granule."""
+    n = (1 << 23) + 3 if dtype == torch.float32 else (1 << 24) + 5
+    x = workloads.random_rows(1, n, dtype, 3, style="normal")
+    assert_parity(x, 4096, sorted_index=True, return_value=True)
+    assert_parity(x, 1, sorted_index=True, return_value=False)
+
+
+def test_values_skipped_and_nonnull_untouched():
+    w = workloads.WORKLOADS["c1"]
+    x = workloads.generate(w).cuda()
+    dstk = _dstk()
+    sentinel = torch.full((w.batch, w.k), -12345.0, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx = torch.empty((w.batch, w.k), dtype=torch.int32, device="cuda")
+    rc = dstk.ds_topk(x.data_ptr(), dstk.FP32, w.batch, w.length, w.length, w.k, 0, 0,
+                      sentinel.data_ptr(), idx.data_ptr(), flag.data_ptr(), 0)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert (sentinel == -12345.0).all(), "out_values written although return_value == 0"
+    _, oi, _, _ = oracle.topk(x.cpu(), w.k)
+    assert torch.equal(torch.sort(idx.cpu(), dim=1).values, oi)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_nan_flag_and_clean_rows_exact(dtype):
+    for length in (4096, 300000):
+        x = workloads.random_rows(6, length, dtype, 21, style="normal")
+        x[0, 0] = float("nan")
+        x[1, length // 2] = float("nan")
+        x[2, length - 1] = float("nan")
+        x[3, length // 3:] = float("-inf")
+        x[3, length - 2] = float("nan")       # NaN inside a -inf tail
+        x[4, 3] = -float("nan")               # negative NaN never beats any threshold
+        gv, gi, gf = run_gpu(x, 64, True, True)
+        assert gf & 1
+        assert_parity(x, 64, True, True, gpu_out=(gv, gi, gf))  # rows 0-4 skipped, row 5 exact
+        clean = workloads.random_rows(2, length, dtype, 22, style="normal")
+        _, _, gf2 = run_gpu(clean, 64, True, True)
+        assert gf2 == 0
+
+
+def test_flag_is_sticky_and_not_cleared():
+    dstk = _dstk()
+    x = workloads.random_rows(2, 1000, torch.float32, 1).cuda()
+    flag = torch.full((1,), 4, dtype=torch.int32, device="cuda")  # caller's own bit
+    dstk.topk(x, 10, nan_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 4
+
+
+def test_batch_zero_and_stream():
+    dstk = _dstk()
+    rc = dstk.ds_topk(0, dstk.BF16, 0, 100, 128, 5, 0, 0, None, 0, 0, 0)
+    assert rc == dstk.OK
+    s = torch.cuda.Stream()
+    x = workloads.random_rows(4, 5000, torch.bfloat16, 9)
+    with torch.cuda.stream(s):
+        gv, gi, gf = run_gpu(x, 300, False, True, stream=s)
+    assert_parity(x, 300, False, True, gpu_out=(gv, gi, gf))
+
+
+def test_invariants_on_gpu_output_c3():
+    w = workloads.WORKLOADS["c3"]
+    x = workloads.generate(w)
+    gv, gi, gf = run_gpu(x, w.k, True, True)
+    for b in range(w.batch):
+        check_invariants(x[b], w.k, gi[b].numpy(), bits_of(gv[b]))
