@@ -19,7 +19,6 @@
 namespace {
 
 using ds_topk_dev::kGranuleCap;
-using ds_topk_dev::kMiscWords;
 using ds_topk_dev::kRadix;
 using ds_topk_dev::kThreads;
 using ds_topk_dev::Params;
@@ -30,9 +29,10 @@ constexpr int kMaxCluster = 16;
 constexpr int64_t kSplitMinRowBytes = 64 * 1024;
 // A CTA of a split row gets at least this many bytes of it.
 constexpr int64_t kMinSliceBytes = 16 * 1024;
-// Bounds of the per-CTA shared-memory copy of the listed granules (16-byte vectors).
-constexpr int64_t kCacheMinVecs = 512;
-constexpr int64_t kCacheMaxVecs = 4096;
+// Dynamic shared memory one CTA may use (B300: 227 KB).
+constexpr int64_t kSmemLimit = 227 * 1024;
+// Most vectors per thread held in the next-row prefetch buffer.
+constexpr int64_t kMaxStageVecs = 16;
 
 struct Plan {
   ds_topk_plan_t pub;
@@ -55,7 +55,7 @@ int validate_sizes(int dtype, int64_t batch, int64_t len, int64_t row_stride, in
 
 // Pure host planning: how the rows map onto CTAs and clusters.
 int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, int sm_count,
-              int max_cluster, Plan* out) {
+              int max_cluster, bool stage, Plan* out) {
   const int rc = validate_sizes(dtype, batch, len, row_stride, k);
   if (rc != DS_TOPK_OK) return rc;
   if (sm_count < 1) return DS_TOPK_EINVAL;
@@ -84,16 +84,45 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
   }
   const int64_t grid = batch * S;
   if (grid > INT32_MAX) return DS_TOPK_EINVAL;
-  // Shared-memory copy of the granules that pass the threshold: about k of them
-  // for data without heavy ties; more (ties, sorted rows) fall back to L2 reads.
-  int64_t cache_vecs = 2 * static_cast<int64_t>(k);
-  if (cache_vecs < kCacheMinVecs) cache_vecs = kCacheMinVecs;
-  if (cache_vecs > kCacheMaxVecs) cache_vecs = kCacheMaxVecs;
-  if (cache_vecs > vec_per_cta) cache_vecs = vec_per_cta;
-  // Dense candidate array: typically about k entries (one per listed granule).
-  int64_t cand_cap = 2 * cache_vecs;
-  if (cand_cap > vec_per_cta * vec) cand_cap = vec_per_cta * vec;
-  const int64_t smem = ds_topk_dev::smem_bytes(g_cap_pad, cache_vecs, cand_cap);
+  // Per-warp granule lists (warp w owns granules [w*segm, (w+1)*segm) of the slice).
+  const int64_t segm = ((ceil_div(g_cap, ds_topk_dev::kWarps) + 31) / 32) * 32;
+  const int64_t list_cap = ds_topk_dev::kWarps * segm;
+  // Candidate regions, one per warp: about k*(1+small)/S candidates per CTA for
+  // data without heavy ties; a region that overflows sends the row to the
+  // fallback path (selection over the listed granules, re-read from L2).
+  int64_t wcap = ceil_div(4 * static_cast<int64_t>(k), ds_topk_dev::kWarps * S);
+  if (wcap < 64) wcap = 64;
+  wcap = (wcap + 31) / 32 * 32;
+  int64_t cand_cap = ds_topk_dev::kWarps * wcap;
+  // The cluster leader gathers every CTA's candidates of the row.
+  const int64_t gath_cap = S > 1 ? 2 * static_cast<int64_t>(k) + 256 : 0;
+  // Next-row prefetch (only useful when a CTA walks several rows): up to 16
+  // vectors per thread, copied with cp.async while the current row is selected.
+  // The listed vectors that the streaming pass copies for the candidate pass
+  // (threshold-guess rows only, i.e. with the prefetch): ~k*(1+small) per CTA.
+  int64_t stage_vecs = 0, lvec_cap = 0;
+  if (gv == 1) {
+    lvec_cap = (ceil_div(2 * static_cast<int64_t>(k), ds_topk_dev::kWarps * S) + 31) / 32 * 32;
+    if (lvec_cap < 64) lvec_cap = 64;
+    if (lvec_cap > segm) lvec_cap = segm;
+  }
+  if (stage && gv == 1) {
+    stage_vecs = ceil_div(vec_per_cta, kThreads);
+    if (stage_vecs > kMaxStageVecs) stage_vecs = kMaxStageVecs;
+  }
+  auto size = [&]() {
+    return ds_topk_dev::smem_bytes(g_cap_pad, list_cap, cand_cap, gath_cap, stage_vecs, lvec_cap);
+  };
+  int64_t smem = size();
+  while (smem > kSmemLimit && stage_vecs > 0) {
+    stage_vecs /= 2;
+    smem = size();
+  }
+  while (smem > kSmemLimit && cand_cap > ds_topk_dev::kWarps * 64) {
+    cand_cap /= 2;
+    smem = size();
+  }
+  if (smem > kSmemLimit) return DS_TOPK_EINVAL;
 
   out->es = es;
   ds_topk_plan_t& pl = out->pub;
@@ -116,8 +145,11 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
   p.g_total = g_total;
   p.gv = static_cast<int32_t>(gv);
   p.g_cap_pad = static_cast<int32_t>(g_cap_pad);
-  p.cache_vecs = static_cast<int32_t>(cache_vecs);
+  p.list_cap = static_cast<int32_t>(list_cap);
   p.cand_cap = static_cast<int32_t>(cand_cap);
+  p.gath_cap = static_cast<int32_t>(gath_cap);
+  p.stage_vecs = static_cast<int32_t>(stage_vecs);
+  p.lvec_cap = static_cast<int32_t>(lvec_cap);
   p.k = k;
   p.return_value = 0;
   p.out_values = nullptr;
@@ -135,9 +167,7 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 
-constexpr int kMaxSmem =
-    static_cast<int>(ds_topk_dev::smem_bytes(kGranuleCap, kCacheMaxVecs, 2 * kCacheMaxVecs));
-static_assert(kMaxSmem <= 227 * 1024, "shared memory per CTA");
+constexpr int kMaxSmem = static_cast<int>(kSmemLimit);
 
 template <int ES, int S>
 cudaError_t prepare_kernel() {
@@ -309,8 +339,25 @@ extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int
   rc = device_info(&dev);
   if (rc != DS_TOPK_OK) return rc;
   Plan pl;
-  rc = make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, &pl);
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  // With the next-row prefetch, if more rows than co-resident clusters (so that a
+  // persistent cluster walks several rows); otherwise without it.
+  rc = make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, false, &pl);
   if (rc != DS_TOPK_OK) return rc;
+  int resident = resident_cached(dev_id, pl.es, pl.pub.cluster_size, pl.pub.smem_bytes, dev.sm_count);
+  if (resident > 0 && batch > resident) {
+    Plan ps;
+    if (make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, true, &ps) ==
+            DS_TOPK_OK &&
+        ps.prm.stage_vecs > 0) {
+      const int rs = resident_cached(dev_id, ps.es, ps.pub.cluster_size, ps.pub.smem_bytes, dev.sm_count);
+      if (rs > 0 && batch > rs) {
+        pl = ps;
+        resident = rs;
+      }
+    }
+  }
   pl.prm.x = static_cast<const char*>(x);
   pl.prm.return_value = return_value;
   pl.prm.out_values = return_value ? out_values : nullptr;
@@ -318,10 +365,6 @@ extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int
   pl.prm.flag = nan_flag;
   // Persistent launch: no more clusters than can be resident at once; each one
   // walks the rows with a stride (and reuses its threshold from row to row).
-  int dev_id = 0;
-  cudaGetDevice(&dev_id);
-  const int resident = resident_cached(dev_id, pl.es, pl.pub.cluster_size, pl.pub.smem_bytes,
-                                       dev.sm_count);
   if (resident > 0 && batch > resident) pl.pub.grid_ctas = static_cast<int64_t>(resident) * pl.pub.cluster_size;
 
   const cudaError_t e = es == 2 ? launch_dtype<2>(pl, stream) : launch_dtype<4>(pl, stream);
@@ -337,7 +380,7 @@ extern "C" int ds_topk_plan(int dtype, int64_t batch, int64_t len, int64_t row_s
                             int sm_count, ds_topk_plan_t* plan) {
   if (!plan) return DS_TOPK_EINVAL;
   Plan pl;
-  const int rc = make_plan(dtype, batch, len, row_stride, k, sm_count, kMaxCluster, &pl);
+  const int rc = make_plan(dtype, batch, len, row_stride, k, sm_count, kMaxCluster, false, &pl);
   if (rc == DS_TOPK_OK) *plan = pl.pub;
   return rc;
 }

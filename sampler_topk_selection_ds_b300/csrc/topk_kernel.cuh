@@ -62,9 +62,12 @@ struct Params {
   int64_t vec_per_cta;   // vectors per CTA slice
   int64_t g_total;       // granules per row, summed over the cluster
   int32_t gv;            // vectors per granule
-  int32_t g_cap_pad;     // per-CTA granule array size (multiple of 8)
-  int32_t cache_vecs;    // capacity of the shared-memory copy of listed granules (vectors)
-  int32_t cand_cap;      // capacity of the dense candidate array (elements)
+  int32_t g_cap_pad;     // per-CTA granule-maximum array size (multiple of 8)
+  int32_t list_cap;      // per-CTA granule list size (kWarps segments)
+  int32_t cand_cap;      // per-CTA candidate capacity (kWarps equal regions)
+  int32_t gath_cap;      // leader's gathered-candidate capacity (clusters only)
+  int32_t stage_vecs;    // vectors per thread prefetched for the next row (0: none)
+  int32_t lvec_cap;      // per-warp copies of listed vectors kept by the streaming pass
   int32_t k;
   int32_t return_value;
   void* out_values;
@@ -312,49 +315,55 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v) {
   return inc - v;
 }
 
-// Shared-memory footprint of one CTA (bytes) for a plan.
-__host__ __device__ constexpr int64_t smem_bytes(int64_t g_cap_pad, int64_t cache_vecs,
-                                                 int64_t cand_cap) {
-  return g_cap_pad * 2 * 2 + (3 * kRadix + kMiscWords) * 4 + cache_vecs * 16 + cand_cap * 8 +
-         ((cache_vecs + 15) & ~int64_t(15));
+
+// Store a u32 at the same shared-memory offset in cluster CTA `rank`.
+__device__ __forceinline__ void dsmem_st_u32(uint32_t* local, uint32_t rank, uint32_t v) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
 }
+
+// misc[] layout (u32 words)
+constexpr int kBc = 0;        // [0..2]   level result: digit, above, found
+constexpr int kXchg = 4;      // [4..7]   cluster exchange: gt, eq, listed count, max key
+constexpr int kOver = 8;      // [8..9]   per-parity overflow counters of windowed levels
+constexpr int kWtot = 16;     // [16..31] per-warp totals (2 x kWarps)
+constexpr int kSegBase = 32;  // [32..39] candidate segment start per warp
+constexpr int kSegCnt = 40;   // [40..47] candidate segment length per warp
+constexpr int kLcnt = 48;     // [48..55] listed granules per warp
+constexpr int kFlagW = 56;    // [56]     CTA flags (bit 0: a candidate region overflowed)
+constexpr int kPub = 64;      // [64..79] counts published to the cluster (per warp + flags)
+constexpr int kAll = 80;      // [80..80+16*kMaxCluster) counts gathered from every CTA
+constexpr int kMaxCluster = 16;
+constexpr int kMiscTotal = kAll + 16 * kMaxCluster;
+
+// Shared-memory footprint of one CTA (bytes) for a plan.
+// Layout: stage | listed vectors | list | union(M, candidates) | gathered | hist | misc.
+// M (granule maxima) is dead once the list is built, before candidates exist.
+__host__ __device__ constexpr int64_t union_bytes(int64_t g_cap_pad, int64_t cand_cap) {
+  return ((g_cap_pad * 2 > cand_cap * 8 ? g_cap_pad * 2 : cand_cap * 8) + 15) & ~int64_t(15);
+}
+__host__ __device__ constexpr int64_t smem_bytes(int64_t g_cap_pad, int64_t list_cap,
+                                                 int64_t cand_cap, int64_t gath_cap,
+                                                 int64_t stage_vecs, int64_t lvec_cap) {
+  return stage_vecs * kThreads * 16 + lvec_cap * kWarps * 16 +
+         ((list_cap * 2 + 15) & ~int64_t(15)) + union_bytes(g_cap_pad, cand_cap) + gath_cap * 8 +
+         (3 * kRadix + kMiscTotal) * 4;
+}
+
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Threshold reuse across rows: a persistent CTA (or cluster) first tries the
 // previous row's threshold lowered by this many top-16 key units; the guess is
 // kept only if it provably holds for the new row (at least k granule maxima
 // reach it) and is not too loose (at most max(2k, k + 1024) of them do).
 constexpr uint32_t kGuessMargin = 4;
-
-__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src) {
-  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
-// The listed granules' vectors, read either from the CTA's shared-memory copy
-// (when they fit) or again from global memory (L2).
-template <int ES>
-struct ListedVectors {
-  const char* rowp;
-  const uint4* cache;
-  const uint16_t* list;
-  int64_t v0, v1, len;
-  int gv;
-  bool cached;
-
-  // q-th vector of the li-th listed granule; v = its vector index in the row.
-  __device__ __forceinline__ uint4 get(int li, int q, int64_t& v, bool& valid) const {
-    v = v0 + static_cast<int64_t>(list[li]) * gv + q;
-    valid = v < v1;
-    if (cached) return cache[li * gv + q];
-    if (valid) return load_vec<ES>(rowp, v, len);
-    return make_uint4(Traits<ES>::kNegInfWord, Traits<ES>::kNegInfWord, Traits<ES>::kNegInfWord,
-                      Traits<ES>::kNegInfWord);
-  }
-};
 
 // The float value whose order key is `key` (so that, for non-NaN v,
 // v >= value  <=>  key(v) >= key). Keys at or below key(-inf) map to -inf.
@@ -369,6 +378,13 @@ __device__ __forceinline__ float key_threshold_value(uint32_t key) {
     const uint32_t raw = key >= 0x80000000u ? key - 0x80000000u : (0x80000000u | (0x80000000u - key));
     return __uint_as_float(raw);
   }
+}
+
+// fp32 value of a packed maximum's result (bf16 widens exactly).
+template <int ES>
+__device__ __forceinline__ float max_value(uint32_t raw) {
+  if constexpr (ES == 2) return __uint_as_float(raw << 16);
+  return __uint_as_float(raw);
 }
 
 // Bit e set iff element e of the vector is a candidate: not below the
@@ -393,6 +409,24 @@ __device__ __forceinline__ uint32_t cand_mask(const uint4& w, float tval) {
   return m;
 }
 
+// Candidate storage: word 0 carries what the order needs, word 1 the index.
+// bf16: key in the low half, input bits in the high half; fp32: input bits.
+template <int ES>
+__device__ __forceinline__ uint32_t cand_pack(uint32_t bits) {
+  if constexpr (ES == 2) return key_of<2>(bits) | (bits << 16);
+  return bits;
+}
+template <int ES>
+__device__ __forceinline__ uint32_t cand_key(uint32_t w0) {
+  if constexpr (ES == 2) return w0 & 0xFFFFu;
+  return key_of<4>(w0);
+}
+template <int ES>
+__device__ __forceinline__ uint32_t cand_bits(uint32_t w0) {
+  if constexpr (ES == 2) return w0 >> 16;
+  return w0;
+}
+
 // 8 consecutive u16 granule maxima starting at `base` (a multiple of 8).
 __device__ __forceinline__ void load_m8(const uint16_t* M, int base, uint32_t m[8]) {
   const uint4 q = *reinterpret_cast<const uint4*>(M + base);
@@ -402,44 +436,31 @@ __device__ __forceinline__ void load_m8(const uint16_t* M, int base, uint32_t m[
   m[6] = q.w & 0xFFFFu; m[7] = q.w >> 16;
 }
 
-// Bit e set iff M[base+e] >= t16 and base+e < end.
-__device__ __forceinline__ uint32_t m8_mask(const uint16_t* M, int base, int end, uint32_t t16) {
-  if (base >= end) return 0u;
-  uint32_t m[8];
-  load_m8(M, base, m);
-  uint32_t mask = 0;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) mask |= static_cast<uint32_t>(base + e < end && m[e] >= t16) << e;
-  return mask;
-}
-
-// misc[] layout (u32 words)
-constexpr int kBc = 0;        // [0..2] level result: digit, above, found
-constexpr int kXchg = 4;      // [4..7] cluster exchange: gt, eq, granule count, max key
-constexpr int kOver = 8;      // [8..9] per-parity overflow counters of windowed levels
-constexpr int kWtot = 16;     // [16..16+2*kWarps) per-warp totals
-
 template <int ES, int S>
-__global__ void __launch_bounds__(kThreads, 3) topk_rows_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) {
   using T = Traits<ES>;
   constexpr int VEC = T::kVec;
   constexpr int KB = T::kKeyBits;
   constexpr uint32_t kFull = 0xFFFFFFFFu;
-  static_assert(kWtot + 2 * kWarps <= kMiscWords, "misc layout");
+  using VT = typename std::conditional<ES == 2, uint16_t, uint32_t>::type;
 
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint16_t* M = reinterpret_cast<uint16_t*>(smem_raw);
-  uint16_t* list = M + p.g_cap_pad;
-  uint32_t* hist = reinterpret_cast<uint32_t*>(list + p.g_cap_pad);  // 2 x kRadix
-  uint32_t* hsum = hist + 2 * kRadix;                                 // kRadix
-  uint32_t* misc = hsum + kRadix;                                     // kMiscWords
+  // next-row prefetch: slot (i, thread) holds step i of the thread's P1 vectors
+  uint4* stage = reinterpret_cast<uint4*>(smem_raw);                            // stage_vecs*kThreads
+  uint4* lvec = stage + p.stage_vecs * kThreads;                                // lvec_cap*kWarps
+  uint16_t* list = reinterpret_cast<uint16_t*>(lvec + p.lvec_cap * kWarps);     // list_cap
+  unsigned char* uni = reinterpret_cast<unsigned char*>(list) + ((p.list_cap * 2 + 15) & ~15);
+  uint16_t* M = reinterpret_cast<uint16_t*>(uni);                               // g_cap_pad
+  uint32_t* cw0 = reinterpret_cast<uint32_t*>(uni);                             // cand_cap
+  uint32_t* cw1 = cw0 + p.cand_cap;                                             // cand_cap
+  uint32_t* gw0 = reinterpret_cast<uint32_t*>(uni + union_bytes(p.g_cap_pad, p.cand_cap));  // gath_cap
+  uint32_t* gw1 = gw0 + p.gath_cap;                                             // gath_cap
+  uint32_t* hist = gw1 + p.gath_cap;                                            // 2 x kRadix
+  uint32_t* hsum = hist + 2 * kRadix;                                           // kRadix
+  uint32_t* misc = hsum + kRadix;                                               // kMiscTotal
   uint32_t* bc = misc + kBc;
   uint32_t* xchg = misc + kXchg;
   uint32_t* wtot = misc + kWtot;
-  uint4* cache = reinterpret_cast<uint4*>(misc + kMiscWords);         // cache_vecs
-  uint32_t* craw = reinterpret_cast<uint32_t*>(cache + p.cache_vecs); // cand_cap raw bits
-  uint32_t* cidx = craw + p.cand_cap;                                 // cand_cap indices
-  uint8_t* vmask = reinterpret_cast<uint8_t*>(cidx + p.cand_cap);     // cache_vecs masks
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -454,335 +475,484 @@ __global__ void __launch_bounds__(kThreads, 3) topk_rows_kernel(const Params p) 
   const int G = static_cast<int>((nv + gv - 1) / gv);
   const uint32_t k = static_cast<uint32_t>(p.k);
   const int64_t row_step = gridDim.x / S;
-  // warp segments of the granule array, 256 granules (8 per lane) per step
-  const int segm = ((G + kWarps - 1) / kWarps + 255) & ~255;
+  // Warp w owns the contiguous granule segment [sb, se); its lanes interleave
+  // (granule sb + 32 i + lane), so every warp load is 512 contiguous bytes and
+  // the warp's list and candidates come out in index order.
+  const int segm = round_up32((G + kWarps - 1) / kWarps);
   const int sb = min(warp * segm, G);
   const int se = min(sb + segm, G);
+  uint16_t* wlist = list + warp * segm;
+  uint4* wvec = lvec + warp * p.lvec_cap;
+  const int wcap = p.cand_cap / kWarps;
+  uint32_t* wc0 = cw0 + warp * wcap;
+  uint32_t* wc1 = cw1 + warp * wcap;
+  // granules whose vectors all lie inside [0, len) (gv == 1: full vectors)
+  const int Gf = gv == 1 ? static_cast<int>(min(v1, max(v0, p.len / VEC)) - v0) : G;
 
   bool have_guess = false;
   uint32_t t_guess = 0;
+  // Steps of the P1 walk whose vectors are prefetched into shared memory with
+  // cp.async while the previous row is being selected (each thread copies and
+  // later reads only its own slots, so no barrier is needed around them).
+  const int nsteps = (se - sb + 31) / 32;
+  const int nstage = gv == 1 ? min(p.stage_vecs, nsteps) : 0;
+  auto prefetch = [&](int64_t r) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + r * p.row_stride_bytes) + v0;
+    for (int i = 0; i < nstage; ++i) {
+      const int g = sb + 32 * i + lane;
+      if (g < min(se, Gf)) cp_async_16(stage + i * kThreads + tid, src + g);
+    }
+    cp_async_commit();
+  };
+  if (nstage > 0 && blockIdx.x / S < p.batch) prefetch(blockIdx.x / S);
 
 #pragma unroll 1
   for (int64_t row = blockIdx.x / S; row < p.batch; row += row_step) {
     const char* rowp = p.x + row * p.row_stride_bytes;
+    const uint4* rowv = reinterpret_cast<const uint4*>(rowp);
     if (tid == 0) {  // level results start defined even if a NaN row breaks the counts
       bc[0] = 0;
       bc[1] = 0;
       bc[2] = 0;
     }
 
-    // ---- P1: granule maxima + NaN test ------------------------------------------
-    uint32_t nan_acc = T::kNegInfWord;  // NaN-propagating running max of everything seen
-    uint32_t mmax = 0;                  // largest granule key seen by this thread
-    if (gv == 1) {
-      // vectors entirely inside [0, len) take the batched 16-byte path; the one
-      // ragged vector at the end of the row (if any) is read element by element.
-      const int64_t full_end = min(v1, max(v0, p.len / VEC));
-      const int Gf = static_cast<int>(full_end - v0);
-      constexpr int U = 8;
-      const uint4* base = reinterpret_cast<const uint4*>(rowp) + v0;
-      for (int g0 = tid; g0 < Gf; g0 += kThreads * U) {
-        uint4 w[U];
+    // ---- P1: one streaming pass over the slice -----------------------------------
+    // guess mode: a granule whose maximum reaches the guessed threshold goes to the
+    //             warp's list right away (nothing else is stored);
+    // exact mode: every granule's maximum key goes to M.
+    // Both modes test every element for NaN through the NaN-propagating maxima.
+    uint32_t t16 = 0;
+    int lc = 0;  // granules in this warp's list (warp-uniform)
+    bool vec_kept = false;  // the list's vectors were copied to wvec by the streaming pass
+    int lvl = 0;
+    bool guess_mode = have_guess;
+#pragma unroll 1
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      uint32_t nan_acc = T::kNegInfWord;
+      uint32_t mmax = 0;
+      const float tg = key_threshold_value<ES>((KB == 16) ? t_guess : (t_guess << 16));
+      lc = 0;
+      if (gv == 1) {
+        constexpr int U = 8;
+        const bool staged = attempt == 0 && nstage > 0;
+        if (staged) cp_async_wait_all();
+        const bool next = staged && row + row_step < p.batch;
+        const uint4* nsrc = reinterpret_cast<const uint4*>(p.x + (row + row_step) * p.row_stride_bytes) + v0;
+        for (int i0 = 0; i0 < nsteps; i0 += U) {
+          uint4 w[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int g = g0 + u * kThreads;
-          if (g < Gf) w[u] = ld_nc_v4(base + g);
-        }
+          for (int u = 0; u < U; ++u) {
+            const int i = i0 + u;
+            const int g = sb + 32 * i + lane;
+            if (g < min(se, Gf)) {
+              if (staged && i < nstage) {
+                w[u] = stage[i * kThreads + tid];
+              } else {
+                w[u] = ld_nc_v4(rowv + (v0 + g));
+              }
+            } else if (g < se) {
+              w[u] = load_vec<ES>(rowp, v0 + g, p.len);  // ragged last vector
+            }
+          }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int g = g0 + u * kThreads;
-          if (g < Gf) {
-            const uint32_t acc = max_acc<ES>(T::kNegInfWord, w[u]);
+          for (int u = 0; u < U; ++u) {
+            const int g = sb + 32 * (i0 + u) + lane;
+            const bool ok = g < se;
+            const uint32_t acc = ok ? max_acc<ES>(T::kNegInfWord, w[u]) : T::kNegInfWord;
+            // the slot's value is in registers and consumed: refill it for the next row
+            if (next && i0 + u < nstage && g < min(se, Gf))
+              cp_async_16(stage + (i0 + u) * kThreads + tid, nsrc + g);
             nan_acc = max_packed<ES>(nan_acc, acc);
-            const uint32_t mk = key_of<ES>(finish_max<ES>(acc)) >> (KB - 16);
+            const uint32_t raw = finish_max<ES>(acc);
+            if (guess_mode) {
+              const bool pass = ok && !(max_value<ES>(raw) < tg);
+              const uint32_t b = __ballot_sync(kFull, pass);
+              if (pass) {
+                const int pos = lc + __popc(b & lt_mask);
+                wlist[pos] = static_cast<uint16_t>(g);
+                if (pos < p.lvec_cap) wvec[pos] = w[u];  // the candidate pass reads it back
+              }
+              lc += __popc(b);
+            } else if (ok) {
+              const uint32_t mk = key_of<ES>(raw) >> (KB - 16);
+              mmax = max(mmax, mk);
+              M[g] = static_cast<uint16_t>(mk);
+            }
+          }
+        }
+        if (next) cp_async_commit();
+      } else {
+        for (int i0 = sb; i0 < se; i0 += 32) {
+          const int g = i0 + lane;
+          const bool ok = g < se;
+          uint32_t acc = T::kNegInfWord;
+          if (ok) {
+            const int64_t vb = v0 + static_cast<int64_t>(g) * gv;
+            const int64_t ve = min(vb + gv, v1);
+            for (int64_t v = vb; v < ve; ++v) acc = max_acc<ES>(acc, load_vec<ES>(rowp, v, p.len));
+          }
+          nan_acc = max_packed<ES>(nan_acc, acc);
+          const uint32_t raw = finish_max<ES>(acc);
+          if (guess_mode) {
+            const bool pass = ok && !(max_value<ES>(raw) < tg);
+            const uint32_t b = __ballot_sync(kFull, pass);
+            if (pass) wlist[lc + __popc(b & lt_mask)] = static_cast<uint16_t>(g);
+            lc += __popc(b);
+          } else if (ok) {
+            const uint32_t mk = key_of<ES>(raw) >> (KB - 16);
             mmax = max(mmax, mk);
             M[g] = static_cast<uint16_t>(mk);
           }
         }
       }
-      if (tid == 0 && Gf < G) {
-        const uint32_t acc = max_acc<ES>(T::kNegInfWord, load_vec<ES>(rowp, full_end, p.len));
-        nan_acc = max_packed<ES>(nan_acc, acc);
-        const uint32_t mk = key_of<ES>(finish_max<ES>(acc)) >> (KB - 16);
-        mmax = max(mmax, mk);
-        M[Gf] = static_cast<uint16_t>(mk);
+      mmax = __reduce_max_sync(kFull, mmax);
+      if (lane == 0) {
+        wtot[warp] = mmax;
+        misc[kLcnt + warp] = static_cast<uint32_t>(lc);
       }
-    } else {
-      for (int g = tid; g < G; g += kThreads) {
-        const int64_t vb = v0 + static_cast<int64_t>(g) * gv;
-        const int64_t ve = min(vb + gv, v1);
-        uint32_t acc = T::kNegInfWord;
-        for (int64_t v = vb; v < ve; ++v) acc = max_acc<ES>(acc, load_vec<ES>(rowp, v, p.len));
-        nan_acc = max_packed<ES>(nan_acc, acc);
-        const uint32_t mk = key_of<ES>(finish_max<ES>(acc)) >> (KB - 16);
-        mmax = max(mmax, mk);
-        M[g] = static_cast<uint16_t>(mk);
-      }
-    }
-    mmax = __reduce_max_sync(kFull, mmax);
-    if (lane == 0) wtot[warp] = mmax;
-    if (__syncthreads_or(is_nan_bits<ES>(finish_max<ES>(nan_acc))) && tid == 0)
-      atomicOr(p.flag, DS_TOPK_FLAG_NAN);
-    mmax = 0;
-    for (int w = 0; w < kWarps; ++w) mmax = max(mmax, wtot[w]);
+      if (__syncthreads_or(is_nan_bits<ES>(finish_max<ES>(nan_acc))) && tid == 0)
+        atomicOr(p.flag, DS_TOPK_FLAG_NAN);
 
-    // ---- A: safe threshold t16 (at least k granule maxima reach it) -----------------
-    int lvl = 0;
-    uint32_t t16 = 0;
-    bool accepted = false;
-    if (have_guess) {
-      t16 = t_guess;
-      uint32_t wcount = 0;
-      for (int b0 = sb; b0 < se; b0 += 256) wcount += __popc(m8_mask(M, b0 + lane * 8, se, t16));
-      wcount = warp_sum(wcount);
-      __syncthreads();  // wtot (warp maxima) read by everyone
-      if (lane == 0) wtot[warp] = wcount;
-      __syncthreads();
-      uint32_t total = 0;
-      for (int w = 0; w < kWarps; ++w) total += wtot[w];
-      if constexpr (S > 1) {
-        if (tid == 0) xchg[2] = total;
-        cg::this_cluster().sync();
-        total = cluster_sum<S>(xchg + 2);
+      if (guess_mode) {
+        // keep the guess only if at least k granule maxima reach it (safety) and
+        // not too many do (tightness)
+        uint32_t total = 0;
+        for (int w = 0; w < kWarps; ++w) total += misc[kLcnt + w];
+        if constexpr (S > 1) {
+          if (tid == 0) xchg[2] = total;
+          cg::this_cluster().sync();
+          total = cluster_sum<S>(xchg + 2);
+        }
+        t16 = t_guess;
+        __syncthreads();  // every warp has read the per-warp counts before they change
+        if (total >= k && total <= max(2u * k, k + 1024u)) {
+          vec_kept = gv == 1;
+          break;
+        }
+        guess_mode = false;  // rerun the pass in exact mode
+        continue;
       }
-      const uint32_t cap = max(2u * k, k + 1024u);
-      accepted = total >= k && total <= cap;
-    }
-    if (!accepted && p.g_total >= static_cast<int64_t>(k)) {
-      // the k-th largest granule maximum, from a histogram over the 256 key
-      // values just below the row's largest granule maximum
-      if constexpr (S > 1) {
-        if (tid == 0) xchg[3] = mmax;
-        cg::this_cluster().sync();
+
+      // ---- A: exact threshold t16 = the k-th largest granule maximum ----------------
+      mmax = 0;
+      for (int w = 0; w < kWarps; ++w) mmax = max(mmax, wtot[w]);
+      t16 = 0;
+      if (p.g_total >= static_cast<int64_t>(k)) {
+        // histogram over the 256 key values just below the row's largest maximum
+        if constexpr (S > 1) {
+          if (tid == 0) xchg[3] = mmax;
+          cg::this_cluster().sync();
 #pragma unroll 1
-        for (int r = 0; r < S; ++r) mmax = max(mmax, dsmem_ld_u32(xchg + 3, static_cast<uint32_t>(r)));
-      }
-      const uint32_t wbase = mmax > 255u ? mmax - 255u : 0u;
-      uint32_t* h = hist + (lvl & 1) * kRadix;
-      uint32_t* ov = misc + kOver + (lvl & 1);
-      if (tid < kRadix) h[tid] = 0;
-      if (tid == 0) *ov = 0;
-      __syncthreads();
-      for (int b0 = sb; b0 < se; b0 += 256) {
-        const int base = b0 + lane * 8;
-        if (base < se) {
-          uint32_t m[8];
-          load_m8(M, base, m);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) hist_add(h, m[e] - wbase, base + e < se && m[e] >= wbase);
+          for (int r = 0; r < S; ++r) mmax = max(mmax, dsmem_ld_u32(xchg + 3, static_cast<uint32_t>(r)));
         }
-      }
-      LevelResult r = finish_level<S>(h, ov, hsum, bc, k);
-      ++lvl;
-      if (r.found) {
-        t16 = wbase + r.digit;
-      } else {
-        // fewer than k maxima within 256 keys of the largest: two 8-bit levels
-        h = hist + (lvl & 1) * kRadix;
-        ov = misc + kOver + (lvl & 1);
+        const uint32_t wbase = mmax > 255u ? mmax - 255u : 0u;
+        uint32_t* h = hist + (lvl & 1) * kRadix;
+        uint32_t* ov = misc + kOver + (lvl & 1);
         if (tid < kRadix) h[tid] = 0;
         if (tid == 0) *ov = 0;
         __syncthreads();
-        for (int b0 = sb; b0 < se; b0 += 256) {
-          const int base = b0 + lane * 8;
-          if (base < se) {
-            uint32_t m[8];
-            load_m8(M, base, m);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) hist_add(h, m[e] >> 8, base + e < se);
-          }
+        for (int g = sb + lane; g < se; g += 32) {
+          const uint32_t m = M[g];
+          hist_add(h, m - wbase, m >= wbase);
         }
-        const LevelResult r1 = finish_level<S>(h, ov, hsum, bc, k);
+        const LevelResult r = finish_level<S>(h, ov, hsum, bc, k);
         ++lvl;
-        const uint32_t d1 = r1.digit, a1 = r1.above;
-        h = hist + (lvl & 1) * kRadix;
-        ov = misc + kOver + (lvl & 1);
-        if (tid < kRadix) h[tid] = 0;
-        if (tid == 0) *ov = 0;
-        __syncthreads();
-        for (int b0 = sb; b0 < se; b0 += 256) {
-          const int base = b0 + lane * 8;
-          if (base < se) {
-            uint32_t m[8];
-            load_m8(M, base, m);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) hist_add(h, m[e] & 0xFFu, base + e < se && (m[e] >> 8) == d1);
-          }
-        }
-        const LevelResult r2 = finish_level<S>(h, ov, hsum, bc, k - a1);
-        ++lvl;
-        t16 = (d1 << 8) | r2.digit;
-      }
-      t_guess = t16 > 0x0080u + kGuessMargin ? t16 - kGuessMargin : 0u;
-      have_guess = true;
-    } else if (!accepted) {
-      t16 = 0;  // fewer granules than k: every element is a candidate
-    }
-
-    // ---- L: ordered list of granules whose maximum reaches t16 ---------------------
-    uint32_t wcount = 0;
-    for (int b0 = sb; b0 < se; b0 += 256) wcount += __popc(m8_mask(M, b0 + lane * 8, se, t16));
-    wcount = warp_sum(wcount);
-    __syncthreads();  // wtot may still be read above
-    if (lane == 0) wtot[warp] = wcount;
-    __syncthreads();
-    int nlist = 0;
-    {
-      uint32_t off = 0;
-      for (int w = 0; w < kWarps; ++w) {
-        const uint32_t t = wtot[w];
-        if (w < warp) off += t;
-        nlist += static_cast<int>(t);
-      }
-      for (int b0 = sb; b0 < se; b0 += 256) {
-        const int base = b0 + lane * 8;
-        uint32_t mask = m8_mask(M, base, se, t16);
-        const uint32_t c = __popc(mask);
-        uint32_t pos = off + warp_excl_scan(c);
-        off += warp_sum(c);
-        while (mask) {
-          const int e = __ffs(mask) - 1;
-          mask &= mask - 1;
-          list[pos++] = static_cast<uint16_t>(base + e);
-        }
-      }
-    }
-    __syncthreads();
-
-    // ---- copy the listed granules into shared memory when they fit -------------------
-    ListedVectors<ES> src;
-    src.rowp = rowp;
-    src.cache = cache;
-    src.list = list;
-    src.v0 = v0;
-    src.v1 = v1;
-    src.len = p.len;
-    src.gv = gv;
-    src.cached = static_cast<int64_t>(nlist) * gv <= p.cache_vecs;
-    if (src.cached) {
-      const int nvecs = nlist * gv;
-      for (int i = tid; i < nvecs; i += kThreads) {
-        int li = i, q = 0;
-        if (gv > 1) {
-          li = i / gv;
-          q = i - li * gv;
-        }
-        const int64_t v = v0 + static_cast<int64_t>(list[li]) * gv + q;
-        if (v < v1 && (v + 1) * VEC <= p.len) {
-          cp_async_16(&cache[i], rowp + v * 16);
+        if (r.found) {
+          t16 = wbase + r.digit;
         } else {
-          // ragged or absent vector: lanes outside [0, len) hold a NaN pattern and
-          // are masked off by index in the candidate test below
-          uint32_t wv[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
-          if (v < v1) {
-            const uint4 f = load_vec<ES>(rowp, v, p.len);
-            const uint32_t fw[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              if (v * VEC + e < p.len) {
-                if constexpr (ES == 2) {
-                  const int sh = (e & 1) * 16;
-                  wv[e >> 1] = (wv[e >> 1] & ~(0xFFFFu << sh)) | (fw[e >> 1] & (0xFFFFu << sh));
-                } else {
-                  wv[e] = fw[e];
-                }
-              }
-            }
+          // fewer than k maxima within 256 keys of the largest: two 8-bit levels
+          h = hist + (lvl & 1) * kRadix;
+          ov = misc + kOver + (lvl & 1);
+          if (tid < kRadix) h[tid] = 0;
+          if (tid == 0) *ov = 0;
+          __syncthreads();
+          for (int g = sb + lane; g < se; g += 32) hist_add(h, M[g] >> 8, true);
+          const LevelResult r1 = finish_level<S>(h, ov, hsum, bc, k);
+          ++lvl;
+          h = hist + (lvl & 1) * kRadix;
+          ov = misc + kOver + (lvl & 1);
+          if (tid < kRadix) h[tid] = 0;
+          if (tid == 0) *ov = 0;
+          __syncthreads();
+          for (int g = sb + lane; g < se; g += 32) {
+            const uint32_t m = M[g];
+            hist_add(h, m & 0xFFu, (m >> 8) == r1.digit);
           }
-          cache[i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          const LevelResult r2 = finish_level<S>(h, ov, hsum, bc, k - r1.above);
+          ++lvl;
+          t16 = (r1.digit << 8) | r2.digit;
         }
+        t_guess = t16 > 0x0080u + kGuessMargin ? t16 - kGuessMargin : 0u;
+        have_guess = true;
       }
-      cp_async_wait_all();
-      __syncthreads();
+      // this warp's list: granules whose maximum reaches t16, in index order
+      lc = 0;
+      for (int i0 = sb; i0 < se; i0 += 32) {
+        const int g = i0 + lane;
+        const bool pass = g < se && M[g] >= t16;
+        const uint32_t b = __ballot_sync(kFull, pass);
+        if (pass) wlist[lc + __popc(b & lt_mask)] = static_cast<uint16_t>(g);
+        lc += __popc(b);
+      }
+      __syncwarp();  // the warp's list is read back by other lanes below
+      break;
     }
 
+    // ---- D: candidates (key >= t, or NaN) of the listed granules, in index order ----
+    // With one vector per granule the listed vectors sit in the warp's shared
+    // copy (kept by the streaming pass, or fetched now from L2); each lane takes
+    // one granule, and positions come from ballots (almost every listed granule
+    // holds exactly one candidate).
     const uint32_t T_full = (KB == 16) ? t16 : (t16 << 16);
     const float tval = key_threshold_value<ES>(T_full);
-    // Each warp owns a contiguous, index-ordered segment of the list.
-    const int segl = round_up32((nlist + kWarps - 1) / kWarps);
-    const int lb = min(warp * segl, nlist);
-    const int le = min(lb + segl, nlist);
-
-    // ---- D: dense, index-ordered array of the candidates -----------------------------
-    // Candidate = key >= t or NaN. Built from the shared-memory copy with fp32
-    // comparisons against the threshold's value (bf16 widens exactly); the
-    // per-vector candidate masks are kept so the write pass does not retest.
-    bool dense = src.cached;
-    int ncand = 0;
-    if (dense) {
-      uint32_t wc = 0;
-      for (int i = lb + lane; i < le; i += 32) {
-        for (int q = 0; q < gv; ++q) {
-          const int ci = i * gv + q;
-          const int64_t v = v0 + static_cast<int64_t>(list[i]) * gv + q;
-          uint32_t m = cand_mask<ES>(cache[ci], tval);
-          if ((v + 1) * VEC > p.len) {  // ragged last vector of the row (or past it)
-            const int64_t valid = v * VEC < p.len ? p.len - v * VEC : 0;
-            m &= (1u << valid) - 1u;
+    int cc = 0;  // this warp's candidates (may exceed wcap: then only counted)
+    const uint4* slice = rowv + v0;
+    const int nvs = static_cast<int>(nv);  // vectors in this slice
+    const int nfull = gv == 1 ? Gf : static_cast<int>(max(int64_t(0), min(nv, p.len / VEC - v0)));
+    if (gv == 1 && lc <= p.lvec_cap) {
+      if (!vec_kept) {  // fetch the listed vectors into the warp's shared copy
+        for (int j = lane; j < lc; j += 32) {
+          const int v = wlist[j];
+          wvec[j] = v < nfull ? ld_nc_v4(slice + v) : load_vec<ES>(rowp, v0 + v, p.len);
+        }
+        __syncwarp();
+      }
+      for (int j0 = 0; j0 < lc; j0 += 32) {
+        const int j = j0 + lane;
+        uint32_t m = 0;
+        int v = 0;
+        if (j < lc) {
+          v = wlist[j];
+          m = cand_mask<ES>(wvec[j], tval);
+          if (v >= nfull) {  // ragged last vector of the row
+            const int64_t valid = p.len - (v0 + v) * VEC;
+            m &= valid >= VEC ? 0xFFu : ((1u << valid) - 1u);
           }
-          vmask[ci] = static_cast<uint8_t>(m);
-          wc += __popc(m);
+        }
+        const uint32_t c = __popc(m);
+        int excl = 0, tot = 0;
+#pragma unroll 1
+        for (uint32_t t = 1;; ++t) {
+          const uint32_t b = __ballot_sync(kFull, c >= t);
+          if (b == 0) break;
+          excl += __popc(b & lt_mask);
+          tot += __popc(b);
+        }
+        int pos = cc + excl;
+        cc += tot;
+        const uint32_t ibase = static_cast<uint32_t>((v0 + v) * VEC);
+        while (m) {
+          const int e = __ffs(m) - 1;
+          m &= m - 1;
+          if (pos < wcap) {
+            uint32_t bits;
+            if constexpr (ES == 2) bits = reinterpret_cast<const uint16_t*>(wvec + j)[e];
+            else bits = reinterpret_cast<const uint32_t*>(wvec + j)[e];
+            wc0[pos] = cand_pack<ES>(bits);
+            wc1[pos] = ibase + e;
+          }
+          ++pos;
         }
       }
-      wc = warp_sum(wc);
-      if (lane == 0) wtot[kWarps + warp] = wc;
-      __syncthreads();
-      uint32_t base = 0;
-      for (int w = 0; w < kWarps; ++w) {
-        const uint32_t t = wtot[kWarps + w];
-        if (w < warp) base += t;
-        ncand += static_cast<int>(t);
-      }
-      dense = ncand <= p.cand_cap;
-      if (dense) {
-        for (int i0 = lb; i0 < le; i0 += 32) {
-          const int i = i0 + lane;
-          uint32_t c = 0;
-          if (i < le)
-            for (int q = 0; q < gv; ++q) c += __popc(vmask[i * gv + q]);
-          uint32_t pos = base + warp_excl_scan(c);
-          base += warp_sum(c);
-          if (c == 0) continue;
-          const int64_t vg = v0 + static_cast<int64_t>(list[i]) * gv;
-          for (int q = 0; q < gv; ++q) {
-            const int ci = i * gv + q;
-            uint32_t m = vmask[ci];
-            const uint32_t ibase = static_cast<uint32_t>((vg + q) * VEC);
-            while (m) {
-              const int e = __ffs(m) - 1;
-              m &= m - 1;
-              if constexpr (ES == 2) {
-                craw[pos] = reinterpret_cast<const uint16_t*>(cache + ci)[e];
-              } else {
-                craw[pos] = reinterpret_cast<const uint32_t*>(cache + ci)[e];
+    } else {
+      // several vectors per granule: count the granule's candidates, then write
+      // them (vectors re-read), so each lane's output stays in index order
+      auto vec_mask = [&](int v, uint4& w) -> uint32_t {
+        w = v < nfull ? ld_nc_v4(slice + v) : load_vec<ES>(rowp, v0 + v, p.len);
+        uint32_t m = cand_mask<ES>(w, tval);
+        if (v >= nfull) {
+          const int64_t valid = p.len - (v0 + v) * VEC;
+          m &= valid <= 0 ? 0u : (valid >= VEC ? 0xFFu : ((1u << valid) - 1u));
+        }
+        return m;
+      };
+      for (int j0 = 0; j0 < lc; j0 += 32) {
+        const int j = j0 + lane;
+        uint32_t c = 0;
+        int vb = 0, ve = 0;
+        if (j < lc) {
+          vb = static_cast<int>(wlist[j]) * gv;
+          ve = min(vb + gv, nvs);
+          for (int v = vb; v < ve; ++v) {
+            uint4 w;
+            c += __popc(vec_mask(v, w));
+          }
+        }
+        int pos = cc + static_cast<int>(warp_excl_scan(c));
+        cc += static_cast<int>(warp_sum(c));
+        if (c == 0) continue;
+        for (int v = vb; v < ve; ++v) {
+          uint4 w;
+          const uint32_t m = vec_mask(v, w);
+          const uint32_t ibase = static_cast<uint32_t>((v0 + v) * VEC);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            if ((m >> e) & 1u) {
+              if (pos < wcap) {
+                wc0[pos] = cand_pack<ES>(elem_bits<ES>(w, e));
+                wc1[pos] = ibase + e;
               }
-              cidx[pos] = ibase + e;
               ++pos;
             }
           }
         }
       }
-      __syncthreads();  // candidates visible; wtot free again
+    }
+    if (lane == 0) {
+      misc[kSegBase + warp] = static_cast<uint32_t>(warp * wcap);
+      misc[kSegCnt + warp] = static_cast<uint32_t>(min(cc, wcap));
+      wtot[kWarps + warp] = static_cast<uint32_t>(cc);
+      misc[kLcnt + warp] = static_cast<uint32_t>(lc);
+    }
+    const bool cta_over = __syncthreads_or(cc > wcap) != 0;
+
+    // ---- cluster: ship every CTA's candidates to the leader (rank 0) --------------
+    bool dense = !cta_over;
+    bool work_here = true;  // this CTA runs the selection (always, unless a non-leader)
+    if constexpr (S > 1) {
+      if (tid < kWarps) misc[kPub + tid] = wtot[kWarps + tid];
+      if (tid == 0) misc[kPub + kWarps] = cta_over ? 1u : 0u;
+      cg::this_cluster().sync();
+      if (tid < S * (kWarps + 1)) {
+        const int r = tid / (kWarps + 1), j = tid - r * (kWarps + 1);
+        misc[kAll + tid] = dsmem_ld_u32(misc + kPub + j, static_cast<uint32_t>(r));
+      }
+      __syncthreads();
+      uint32_t total = 0, before = 0;
+      bool any_over = false;
+      for (int r = 0; r < S; ++r) {
+        any_over |= misc[kAll + r * (kWarps + 1) + kWarps] != 0u;
+        for (int w = 0; w < kWarps; ++w) {
+          const uint32_t c = misc[kAll + r * (kWarps + 1) + w];
+          if (r < rank || (r == rank && w < warp)) before += c;
+          total += c;
+        }
+      }
+      dense = !any_over && total <= static_cast<uint32_t>(p.gath_cap);
+      if (dense) {
+        const int mine = min(cc, wcap);
+        for (int c = lane; c < mine; c += 32) {
+          dsmem_st_u32(gw0 + before + c, 0u, wc0[c]);
+          dsmem_st_u32(gw1 + before + c, 0u, wc1[c]);
+        }
+        cg::this_cluster().sync();  // the leader's gathered array is complete
+        work_here = rank == 0;
+        if (work_here && lane == 0) {
+          const uint32_t per = (total + kWarps - 1) / kWarps;
+          const uint32_t b = min(static_cast<uint32_t>(warp) * per, total);
+          misc[kSegBase + warp] = b;
+          misc[kSegCnt + warp] = min(b + per, total) - b;
+        }
+        __syncthreads();
+      }
     }
 
-    // ---- B: exact k-th key among the candidates ---------------------------------------
-    // visit(f): calls f(key, valid) for every candidate, warp-uniformly.
-    auto visit = [&](auto&& f) {
-      if (dense) {
-        const int nw = round_up32(ncand);
-        for (int c = tid; c < nw; c += kThreads) {
-          const bool ok = c < ncand;
-          f(key_of<ES>(ok ? craw[c] : 0u), ok);
+    int32_t* out_idx = p.out_indices + row * static_cast<int64_t>(k);
+    VT* out_val = p.return_value ? reinterpret_cast<VT*>(p.out_values) + row * static_cast<int64_t>(k) : nullptr;
+
+    if (dense && work_here) {
+      // ---- B (dense): exact k-th key among the candidates, locally -------------------
+      const uint32_t* c0 = (S > 1) ? gw0 : cw0;
+      const uint32_t* c1 = (S > 1) ? gw1 : cw1;
+      const int sbase = static_cast<int>(misc[kSegBase + warp]);
+      const int scnt = static_cast<int>(misc[kSegCnt + warp]);
+      uint32_t need = k, kstar = 0;
+      uint32_t wbase = t16;
+#pragma unroll 1
+      while (true) {  // windowed level on the top 16 key bits, moving up from t16
+        uint32_t* h = hist + (lvl & 1) * kRadix;
+        uint32_t* ov = misc + kOver + (lvl & 1);
+        if (tid < kRadix) h[tid] = 0;
+        if (tid == 0) *ov = 0;
+        __syncthreads();
+        uint32_t lover = 0;
+        for (int c = lane; c < round_up32(scnt); c += 32) {
+          const bool okc = c < scnt;
+          const uint32_t k16v = cand_key<ES>(okc ? c0[sbase + c] : 0u) >> (KB - 16);
+          const bool ok = okc && k16v >= wbase;
+          const uint32_t d = k16v - wbase;
+          hist_add(h, d, ok && d < 256u);
+          lover += __popc(__ballot_sync(kFull, ok && d >= 256u));
         }
-      } else {
-        const int nw = round_up32(nlist);
-        for (int i = tid; i < nw; i += kThreads) {
-          const bool gok = i < nlist;
+        if (lane == 0 && lover) atomicAdd(ov, lover);
+        const LevelResult r = finish_level<1>(h, ov, hsum, bc, need);
+        ++lvl;
+        if (r.shift && wbase + 256u <= 0xFFFFu) {
+          wbase += 256u;
+          continue;
+        }
+        kstar = (wbase + r.digit) << (KB - 16);
+        need -= r.above;
+        break;
+      }
+      if constexpr (KB == 32) {
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {  // low 16 bits: two 8-bit levels
+          const int shift = 8 - 8 * j;
+          uint32_t* h = hist + (lvl & 1) * kRadix;
+          uint32_t* ov = misc + kOver + (lvl & 1);
+          if (tid < kRadix) h[tid] = 0;
+          if (tid == 0) *ov = 0;
+          __syncthreads();
+          const uint32_t pre = kstar >> (shift + 8);
+          for (int c = lane; c < scnt; c += 32) {
+            const uint32_t key = cand_key<ES>(c0[sbase + c]);
+            hist_add(h, (key >> shift) & 0xFFu, (key >> (shift + 8)) == pre);
+          }
+          const LevelResult r = finish_level<1>(h, ov, hsum, bc, need);
+          ++lvl;
+          kstar |= r.digit << shift;
+          need -= r.above;
+        }
+      }
+      const uint32_t r_ties = need;  // elements equal to K* that are taken
+
+      // ---- C (dense): ordered compaction -------------------------------------------
+      uint32_t c_gt = 0, c_eq = 0;
+      for (int c = lane; c < round_up32(scnt); c += 32) {
+        const uint32_t key = cand_key<ES>(c < scnt ? c0[sbase + c] : 0u);
+        c_gt += __popc(__ballot_sync(kFull, c < scnt && key > kstar));
+        c_eq += __popc(__ballot_sync(kFull, c < scnt && key == kstar));
+      }
+      if (lane == 0) {
+        wtot[warp] = c_gt;
+        wtot[kWarps + warp] = c_eq;
+      }
+      __syncthreads();
+      uint32_t base_gt = 0, base_eq = 0;
+      for (int w = 0; w < warp; ++w) {
+        base_gt += wtot[w];
+        base_eq += wtot[kWarps + w];
+      }
+      for (int c = lane; c < round_up32(scnt); c += 32) {
+        const bool ok = c < scnt;
+        const uint32_t w0 = ok ? c0[sbase + c] : 0u;
+        const uint32_t key = cand_key<ES>(w0);
+        const uint32_t mg = __ballot_sync(kFull, ok && key > kstar);
+        const uint32_t mq = __ballot_sync(kFull, ok && key == kstar);
+        const uint32_t bg = base_gt + __popc(mg & lt_mask);
+        const uint32_t bq = base_eq + __popc(mq & lt_mask);
+        base_gt += __popc(mg);
+        base_eq += __popc(mq);
+        uint32_t pos = 0xFFFFFFFFu;
+        if ((mg >> lane) & 1u) pos = bg + min(bq, r_ties);
+        else if (((mq >> lane) & 1u) && bq < r_ties) pos = bg + bq;
+        if (pos < k) {
+          out_idx[pos] = static_cast<int32_t>(c1[sbase + c]);
+          if (out_val) out_val[pos] = static_cast<VT>(cand_bits<ES>(w0));
+        }
+      }
+    } else if (!dense) {
+      // ---- fallback: candidates did not fit; select over the listed granules, ------
+      // re-read from global memory, with cluster-wide histograms.
+      auto visit = [&](auto&& f) {
+        for (int j = lane; j < round_up32(lc); j += 32) {
+          const bool gok = j < lc;
           for (int q = 0; q < gv; ++q) {
-            int64_t v = 0;
-            bool vok = false;
+            const int64_t v = gok ? v0 + static_cast<int64_t>(wlist[j]) * gv + q : v1;
+            const bool vok = v < v1;
             uint4 w = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
-            if (gok) w = src.get(i, q, v, vok);
+            if (vok) w = load_vec<ES>(rowp, v, p.len);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
               const uint32_t eb = elem_bits<ES>(w, e);
@@ -791,14 +961,8 @@ __global__ void __launch_bounds__(kThreads, 3) topk_rows_kernel(const Params p) 
             }
           }
         }
-      }
-    };
-
-    // Windowed level on the top 16 key bits: bins [wbase, wbase + 256), keys above
-    // the window counted apart. The window starts at t16 (every candidate except a
-    // NaN is at or above it) and moves up until it holds the k-th largest.
-    uint32_t need = k, cnt_gt = 0, kstar = 0;
-    {
+      };
+      uint32_t need = k, kstar = 0;
       uint32_t wbase = t16;
 #pragma unroll 1
       while (true) {
@@ -823,154 +987,86 @@ __global__ void __launch_bounds__(kThreads, 3) topk_rows_kernel(const Params p) 
           continue;
         }
         kstar = (wbase + r.digit) << (KB - 16);
-        cnt_gt += r.above;
         need -= r.above;
         break;
       }
-    }
-    if constexpr (KB == 32) {
-      // the low 16 bits of K*: two 8-bit levels among candidates with its top 16 bits
+      if constexpr (KB == 32) {
 #pragma unroll 1
-      for (int j = 0; j < 2; ++j) {
-        const int shift = 8 - 8 * j;
-        uint32_t* h = hist + (lvl & 1) * kRadix;
-        uint32_t* ov = misc + kOver + (lvl & 1);
-        if (tid < kRadix) h[tid] = 0;
-        if (tid == 0) *ov = 0;
-        __syncthreads();
-        const uint32_t pre = kstar >> (shift + 8);
-        visit([&](uint32_t key, bool ok) {
-          hist_add(h, (key >> shift) & 0xFFu, ok && (key >> (shift + 8)) == pre);
-        });
-        const LevelResult r = finish_level<S>(h, ov, hsum, bc, need);
-        ++lvl;
-        kstar |= r.digit << shift;
-        cnt_gt += r.above;
-        need -= r.above;
+        for (int j = 0; j < 2; ++j) {
+          const int shift = 8 - 8 * j;
+          uint32_t* h = hist + (lvl & 1) * kRadix;
+          uint32_t* ov = misc + kOver + (lvl & 1);
+          if (tid < kRadix) h[tid] = 0;
+          if (tid == 0) *ov = 0;
+          __syncthreads();
+          const uint32_t pre = kstar >> (shift + 8);
+          visit([&](uint32_t key, bool ok) {
+            hist_add(h, (key >> shift) & 0xFFu, ok && (key >> (shift + 8)) == pre);
+          });
+          const LevelResult r = finish_level<S>(h, ov, hsum, bc, need);
+          ++lvl;
+          kstar |= r.digit << shift;
+          need -= r.above;
+        }
       }
-    }
-    const uint32_t r_ties = need;    // how many elements equal to K* are taken
-    const uint32_t k16 = kstar >> (KB - 16);
-
-    // ---- C: ordered compaction of the selected elements -------------------------------
-    // Counts per warp segment, prefix over warps (and over the cluster's CTAs), then
-    // every selected element is written at (#selected elements before it).
-    const int segc = round_up32((ncand + kWarps - 1) / kWarps);
-    const int cb = dense ? min(warp * segc, ncand) : lb;
-    const int ce = dense ? min(cb + segc, ncand) : le;
-    uint32_t c_gt = 0, c_eq = 0;
-    if (dense) {
-      for (int c0 = cb; c0 < ce; c0 += 32) {
-        const int c = c0 + lane;
-        const uint32_t key = key_of<ES>(c < ce ? craw[c] : 0u);
-        c_gt += __popc(__ballot_sync(kFull, c < ce && key > kstar));
-        c_eq += __popc(__ballot_sync(kFull, c < ce && key == kstar));
+      const uint32_t r_ties = need;
+      // counts of this warp's list, then prefixes over warps and cluster CTAs
+      uint32_t c_gt = 0, c_eq = 0;
+      visit([&](uint32_t key, bool ok) {
+        c_gt += __popc(__ballot_sync(kFull, ok && key > kstar));
+        c_eq += __popc(__ballot_sync(kFull, ok && key == kstar));
+      });
+      if (lane == 0) {
+        wtot[warp] = c_gt;
+        wtot[kWarps + warp] = c_eq;
       }
-    } else {
-      for (int i = lb + lane; i < le; i += 32) {
-        if (M[list[i]] < k16) continue;
+      __syncthreads();
+      uint32_t base_gt = 0, base_eq = 0, cta_gt = 0, cta_eq = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        const uint32_t tg = wtot[w], te = wtot[kWarps + w];
+        if (w < warp) {
+          base_gt += tg;
+          base_eq += te;
+        }
+        cta_gt += tg;
+        cta_eq += te;
+      }
+      if constexpr (S > 1) {
+        if (tid == 0) {
+          xchg[0] = cta_gt;
+          xchg[1] = cta_eq;
+        }
+        cg::this_cluster().sync();
+#pragma unroll 1
+        for (int r = 0; r < rank; ++r) {
+          base_gt += dsmem_ld_u32(xchg, static_cast<uint32_t>(r));
+          base_eq += dsmem_ld_u32(xchg + 1, static_cast<uint32_t>(r));
+        }
+      }
+      // write pass: one granule per lane, lanes in index order
+      for (int j0 = 0; j0 < lc; j0 += 32) {
+        const int j = j0 + lane;
+        const bool gok = j < lc;
         for (int q = 0; q < gv; ++q) {
-          int64_t v;
-          bool vok;
-          const uint4 w = src.get(i, q, v, vok);
-          if (!vok) continue;
+          const int64_t v = gok ? v0 + static_cast<int64_t>(wlist[j]) * gv + q : v1;
+          const bool vok = v < v1;
+          uint4 w = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
+          if (vok) w = load_vec<ES>(rowp, v, p.len);
+          uint32_t lg = 0, lq = 0;
 #pragma unroll
           for (int e = 0; e < VEC; ++e) {
             const uint32_t eb = elem_bits<ES>(w, e);
             const uint32_t key = key_of<ES>(eb);
-            if (v * VEC + e < p.len && (key >= T_full || is_nan_bits<ES>(eb))) {
-              c_gt += key > kstar;
-              c_eq += key == kstar;
+            if (vok && v * VEC + e < p.len && (key >= T_full || is_nan_bits<ES>(eb))) {
+              lg += key > kstar;
+              lq += key == kstar;
             }
           }
-        }
-      }
-      c_gt = warp_sum(c_gt);
-      c_eq = warp_sum(c_eq);
-    }
-    if (lane == 0) {
-      wtot[warp] = c_gt;
-      wtot[kWarps + warp] = c_eq;
-    }
-    __syncthreads();
-    uint32_t base_gt = 0, base_eq = 0, cta_gt = 0, cta_eq = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      const uint32_t tg = wtot[w], te = wtot[kWarps + w];
-      if (w < warp) {
-        base_gt += tg;
-        base_eq += te;
-      }
-      cta_gt += tg;
-      cta_eq += te;
-    }
-    if constexpr (S > 1) {
-      if (tid == 0) {
-        xchg[0] = cta_gt;
-        xchg[1] = cta_eq;
-      }
-      cg::this_cluster().sync();
-#pragma unroll 1
-      for (int r = 0; r < rank; ++r) {
-        base_gt += dsmem_ld_u32(xchg, static_cast<uint32_t>(r));
-        base_eq += dsmem_ld_u32(xchg + 1, static_cast<uint32_t>(r));
-      }
-    }
-
-    int32_t* out_idx = p.out_indices + row * static_cast<int64_t>(k);
-    using VT = typename std::conditional<ES == 2, uint16_t, uint32_t>::type;
-    VT* out_val = p.return_value ? reinterpret_cast<VT*>(p.out_values) + row * static_cast<int64_t>(k) : nullptr;
-    if (dense) {
-      for (int c0 = cb; c0 < ce; c0 += 32) {
-        const int c = c0 + lane;
-        const bool ok = c < ce;
-        const uint32_t bits = ok ? craw[c] : 0u;
-        const uint32_t key = key_of<ES>(bits);
-        const uint32_t mg = __ballot_sync(kFull, ok && key > kstar);
-        const uint32_t mq = __ballot_sync(kFull, ok && key == kstar);
-        const uint32_t bg = base_gt + __popc(mg & lt_mask);
-        const uint32_t bq = base_eq + __popc(mq & lt_mask);
-        base_gt += __popc(mg);
-        base_eq += __popc(mq);
-        uint32_t pos = 0xFFFFFFFFu;
-        if ((mg >> lane) & 1u) pos = bg + min(bq, r_ties);
-        else if (((mq >> lane) & 1u) && bq < r_ties) pos = bg + bq;
-        if (pos < k) {
-          out_idx[pos] = static_cast<int32_t>(cidx[c]);
-          if (out_val) out_val[pos] = static_cast<VT>(bits);
-        }
-      }
-    } else {
-      for (int i0 = lb; i0 < le; i0 += 32) {
-        const int i = i0 + lane;
-        const bool live = i < le && M[list[i < le ? i : lb]] >= k16;
-        uint32_t lg = 0, lq = 0;
-        if (live) {
-          for (int q = 0; q < gv; ++q) {
-            int64_t v;
-            bool vok;
-            const uint4 w = src.get(i, q, v, vok);
-            if (!vok) continue;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              const uint32_t eb = elem_bits<ES>(w, e);
-              const uint32_t key = key_of<ES>(eb);
-              if (v * VEC + e < p.len && (key >= T_full || is_nan_bits<ES>(eb))) {
-                lg += key > kstar;
-                lq += key == kstar;
-              }
-            }
-          }
-        }
-        uint32_t bg = base_gt + warp_excl_scan(lg);
-        uint32_t bq = base_eq + warp_excl_scan(lq);
-        base_gt += warp_sum(lg);
-        base_eq += warp_sum(lq);
-        if (lg + lq == 0) continue;
-        for (int q = 0; q < gv; ++q) {
-          int64_t v;
-          bool vok;
-          const uint4 w = src.get(i, q, v, vok);
-          if (!vok) continue;
+          uint32_t bg = base_gt + warp_excl_scan(lg);
+          uint32_t bq = base_eq + warp_excl_scan(lq);
+          base_gt += warp_sum(lg);
+          base_eq += warp_sum(lq);
+          if (lg + lq == 0) continue;
 #pragma unroll
           for (int e = 0; e < VEC; ++e) {
             const int64_t idx = v * VEC + e;
@@ -994,7 +1090,7 @@ __global__ void __launch_bounds__(kThreads, 3) topk_rows_kernel(const Params p) 
         }
       }
     }
-    // the next row reuses every shared buffer; cluster peers may still read xchg
+    // the next row reuses every shared buffer; cluster peers may still read ours
     if constexpr (S > 1) {
       cg::this_cluster().sync();
     } else {
