@@ -87,15 +87,14 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
   // Per-warp granule lists (warp w owns granules [w*segm, (w+1)*segm) of the slice).
   const int64_t segm = ((ceil_div(g_cap, ds_topk_dev::kWarps) + 31) / 32) * 32;
   const int64_t list_cap = ds_topk_dev::kWarps * segm;
-  // Candidate regions, one per warp: about k*(1+small)/S candidates per CTA for
-  // data without heavy ties; a region that overflows sends the row to the
-  // fallback path (selection over the listed granules, re-read from L2).
-  int64_t wcap = ceil_div(4 * static_cast<int64_t>(k), ds_topk_dev::kWarps * S);
-  if (wcap < 64) wcap = 64;
-  wcap = (wcap + 31) / 32 * 32;
-  int64_t cand_cap = ds_topk_dev::kWarps * wcap;
+  // Candidate array of a CTA: about k*(1+small)/S candidates per CTA for data
+  // without heavy ties; a CTA that overflows it sends the row to the fallback
+  // path (selection over the listed granules, re-read from L2).
+  int64_t cand_cap = (ceil_div(4 * static_cast<int64_t>(k), S) + 255) / 256 * 256;
+  if (cand_cap < 512) cand_cap = 512;
   // The cluster leader gathers every CTA's candidates of the row.
-  const int64_t gath_cap = S > 1 ? 2 * static_cast<int64_t>(k) + 256 : 0;
+  // (multiples of 4 entries keep every later shared-memory region 16-byte aligned)
+  const int64_t gath_cap = S > 1 ? (2 * static_cast<int64_t>(k) + 256 + 3) / 4 * 4 : 0;
   // Next-row prefetch (only useful when a CTA walks several rows): up to 16
   // vectors per thread, copied with cp.async while the current row is selected.
   // The listed vectors that the streaming pass copies for the candidate pass
@@ -118,7 +117,7 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
     stage_vecs /= 2;
     smem = size();
   }
-  while (smem > kSmemLimit && cand_cap > ds_topk_dev::kWarps * 64) {
+  while (smem > kSmemLimit && cand_cap > 512) {
     cand_cap /= 2;
     smem = size();
   }

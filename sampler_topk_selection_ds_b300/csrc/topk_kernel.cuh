@@ -223,51 +223,39 @@ __device__ __forceinline__ void row_sync() {
   }
 }
 
-// Sum of a shared u32 over the cluster (after a row_sync made it visible).
-template <int S>
-__device__ __forceinline__ uint32_t cluster_sum(const uint32_t* w) {
-  if constexpr (S > 1) {
-    uint32_t t = 0;
-#pragma unroll 1
-    for (int r = 0; r < S; ++r) t += dsmem_ld_u32(w, static_cast<uint32_t>(r));
-    return t;
-  } else {
-    return *w;
-  }
+// Non-blocking reductions into the same shared-memory word of cluster CTA `rank`.
+__device__ __forceinline__ void dsmem_red_add_u32(uint32_t* local, uint32_t rank, uint32_t v) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
+}
+__device__ __forceinline__ void dsmem_red_max_u32(uint32_t* local, uint32_t rank, uint32_t v) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
 }
 
 struct LevelResult {
   uint32_t digit;  // bin holding the need-th largest key
   uint32_t above;  // keys above that bin (including the window's overflow count)
+  uint32_t count;  // keys in that bin
   bool found;      // false: fewer than `need` keys in the window and above it
   bool shift;      // true: the need-th largest key lies above the window
 };
 
-// Completes one histogram level: makes every CTA's histogram h (256 bins) and
-// overflow count *ov (keys above the window) visible, sums them over the
-// cluster, and locates the bin d with  ov + sum(h[> d]) < need <= ov + sum(h[>= d]).
-template <int S>
-__device__ __forceinline__ LevelResult finish_level(uint32_t* h, uint32_t* ov, uint32_t* hsum,
-                                                    uint32_t* bc, uint32_t need) {
-  row_sync<S>();
+// Locates the bin d with  over + sum(h[> d]) < need <= over + sum(h[>= d])  in a
+// 256-bin histogram h (16-byte aligned) and broadcasts it through bc[0..2].
+// Every thread of the CTA calls it; h and over must already be final.
+__device__ __forceinline__ LevelResult scan_level(const uint32_t* h, uint32_t over, uint32_t* bc,
+                                                  uint32_t need) {
   const int tid = threadIdx.x;
-  if (tid < kRadix) {
-    uint32_t s = 0;
-    if constexpr (S > 1) {
-#pragma unroll 4
-      for (int r = 0; r < S; ++r) s += dsmem_ld_u32(h + tid, static_cast<uint32_t>(r));
-    } else {
-      s = h[tid];
-    }
-    hsum[tid] = s;
-  }
-  const uint32_t over = cluster_sum<S>(ov);
-  __syncthreads();
   if (tid < 32 && over < need) {
     const int lane = tid;
     const uint32_t n2 = need - over;
-    const uint4 c0 = reinterpret_cast<const uint4*>(hsum)[lane * 2];
-    const uint4 c1 = reinterpret_cast<const uint4*>(hsum)[lane * 2 + 1];
+    const uint4 c0 = reinterpret_cast<const uint4*>(h)[lane * 2];
+    const uint4 c1 = reinterpret_cast<const uint4*>(h)[lane * 2 + 1];
     const uint32_t c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
     uint32_t s = 0;
 #pragma unroll
@@ -287,6 +275,7 @@ __device__ __forceinline__ LevelResult finish_level(uint32_t* h, uint32_t* ov, u
         if (run + c[j] >= n2) {
           bc[0] = static_cast<uint32_t>(lane * 8 + j);
           bc[1] = run + over;
+          bc[3] = c[j];
           break;
         }
         run += c[j];
@@ -299,8 +288,57 @@ __device__ __forceinline__ LevelResult finish_level(uint32_t* h, uint32_t* ov, u
   r.found = r.shift || bc[2] != 0u;
   r.digit = bc[0];
   r.above = bc[1];
+  r.count = bc[3];
+  __syncthreads();  // bc may be rewritten by the next level
   return r;
 }
+
+// Histogram levels whose counts are summed over the cluster, by reduce-scatter:
+// bin b belongs to CTA (b mod S); every CTA adds its local count of bin b into
+// the owner's receive histogram (red.shared::cluster, non-blocking), one cluster
+// barrier, then every CTA reads the 256 sums back from their owners (one
+// distributed-shared-memory load per thread) and scans them locally. Receive
+// histograms rotate over three buffers (the level counter runs on across rows,
+// identically in every CTA of the cluster): the buffer a level clears for the
+// next one was last read two levels earlier, before a barrier every CTA has
+// passed, and is next written only after the current level's barrier.
+struct ClusterLevels {
+  uint32_t* hist;  // local kRadix | 3 x received kRadix
+  uint32_t* ovw;   // [0] local overflow, [1..3] received overflow (held by CTA 0)
+  uint32_t* bc;
+  __device__ uint32_t* loc() const { return hist; }
+  __device__ uint32_t* rcv(int lvl) const { return hist + kRadix * (1 + lvl % 3); }
+  __device__ uint32_t* ov() const { return ovw; }
+
+  // Clears the local histogram and overflow word (callers then add).
+  __device__ void begin() const {
+    if (threadIdx.x < kRadix) hist[threadIdx.x] = 0;
+    if (threadIdx.x == 0) ovw[0] = 0;
+    __syncthreads();
+  }
+
+  template <int S>
+  __device__ LevelResult finish(int lvl, uint32_t need) const {
+    __syncthreads();  // local counts complete
+    const int tid = threadIdx.x;
+    if constexpr (S > 1) {
+      if (tid < kRadix) {
+        const uint32_t v = hist[tid];
+        if (v) dsmem_red_add_u32(rcv(lvl) + tid, static_cast<uint32_t>(tid % S), v);
+        rcv(lvl + 1)[tid] = 0;
+      }
+      if (tid == 0) {
+        if (ovw[0]) dsmem_red_add_u32(ovw + 1 + lvl % 3, 0u, ovw[0]);
+        ovw[1 + (lvl + 1) % 3] = 0;
+      }
+      cg::this_cluster().sync();
+      if (tid < kRadix) hist[tid] = dsmem_ld_u32(rcv(lvl) + tid, static_cast<uint32_t>(tid % S));
+      if (tid == 0) ovw[0] = dsmem_ld_u32(ovw + 1 + lvl % 3, 0u);
+      __syncthreads();
+    }
+    return scan_level(hist, ovw[0], bc, need);
+  }
+};
 
 __device__ __forceinline__ uint32_t warp_sum(uint32_t v) { return __reduce_add_sync(0xFFFFFFFFu, v); }
 
@@ -326,20 +364,25 @@ __device__ __forceinline__ void dsmem_st_u32(uint32_t* local, uint32_t rank, uin
 
 // misc[] layout (u32 words)
 constexpr int kBc = 0;        // [0..2]   level result: digit, above, found
-constexpr int kXchg = 4;      // [4..7]   cluster exchange: gt, eq, listed count, max key
-constexpr int kOver = 8;      // [8..9]   per-parity overflow counters of windowed levels
+constexpr int kXmax = 4;      // [4]      cluster: row's largest granule key (pushed max)
+constexpr int kXtot = 5;      // [5]      cluster: listed granules under the guess (pushed sum)
+constexpr int kXpreGt = 6;    // [6]      cluster: selected '>' elements of lower ranks (pushed)
+constexpr int kXpreEq = 7;    // [7]      cluster: '==' elements of lower ranks (pushed)
+constexpr int kOvw = 8;       // [8..11]  overflow words of cluster levels (local + 3 received)
+constexpr int kOvl = 12;      // [12]     overflow word of local levels
 constexpr int kWtot = 16;     // [16..31] per-warp totals (2 x kWarps)
 constexpr int kSegBase = 32;  // [32..39] candidate segment start per warp
 constexpr int kSegCnt = 40;   // [40..47] candidate segment length per warp
 constexpr int kLcnt = 48;     // [48..55] listed granules per warp
-constexpr int kFlagW = 56;    // [56]     CTA flags (bit 0: a candidate region overflowed)
 constexpr int kPub = 64;      // [64..79] counts published to the cluster (per warp + flags)
 constexpr int kAll = 80;      // [80..80+16*kMaxCluster) counts gathered from every CTA
 constexpr int kMaxCluster = 16;
 constexpr int kMiscTotal = kAll + 16 * kMaxCluster;
+constexpr int kHistWords = 5 * kRadix;  // cluster levels: local + 3 received; one local-level histogram
 
 // Shared-memory footprint of one CTA (bytes) for a plan.
-// Layout: stage | listed vectors | list | union(M, candidates) | gathered | hist | misc.
+// Layout: stage | listed vectors | their candidate masks | list | union(M, candidates) |
+// gathered | hist | misc.
 // M (granule maxima) is dead once the list is built, before candidates exist.
 __host__ __device__ constexpr int64_t union_bytes(int64_t g_cap_pad, int64_t cand_cap) {
   return ((g_cap_pad * 2 > cand_cap * 8 ? g_cap_pad * 2 : cand_cap * 8) + 15) & ~int64_t(15);
@@ -347,9 +390,9 @@ __host__ __device__ constexpr int64_t union_bytes(int64_t g_cap_pad, int64_t can
 __host__ __device__ constexpr int64_t smem_bytes(int64_t g_cap_pad, int64_t list_cap,
                                                  int64_t cand_cap, int64_t gath_cap,
                                                  int64_t stage_vecs, int64_t lvec_cap) {
-  return stage_vecs * kThreads * 16 + lvec_cap * kWarps * 16 +
+  return stage_vecs * kThreads * 16 + lvec_cap * kWarps * 16 + ((lvec_cap * kWarps + 15) & ~int64_t(15)) +
          ((list_cap * 2 + 15) & ~int64_t(15)) + union_bytes(g_cap_pad, cand_cap) + gath_cap * 8 +
-         (3 * kRadix + kMiscTotal) * 4;
+         (kHistWords + kMiscTotal) * 4;
 }
 
 __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src) {
@@ -448,19 +491,20 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   // next-row prefetch: slot (i, thread) holds step i of the thread's P1 vectors
   uint4* stage = reinterpret_cast<uint4*>(smem_raw);                            // stage_vecs*kThreads
   uint4* lvec = stage + p.stage_vecs * kThreads;                                // lvec_cap*kWarps
-  uint16_t* list = reinterpret_cast<uint16_t*>(lvec + p.lvec_cap * kWarps);     // list_cap
+  uint8_t* lmask = reinterpret_cast<uint8_t*>(lvec + p.lvec_cap * kWarps);      // lvec_cap*kWarps
+  uint16_t* list = reinterpret_cast<uint16_t*>(lmask + ((p.lvec_cap * kWarps + 15) & ~15));  // list_cap
   unsigned char* uni = reinterpret_cast<unsigned char*>(list) + ((p.list_cap * 2 + 15) & ~15);
   uint16_t* M = reinterpret_cast<uint16_t*>(uni);                               // g_cap_pad
   uint32_t* cw0 = reinterpret_cast<uint32_t*>(uni);                             // cand_cap
   uint32_t* cw1 = cw0 + p.cand_cap;                                             // cand_cap
   uint32_t* gw0 = reinterpret_cast<uint32_t*>(uni + union_bytes(p.g_cap_pad, p.cand_cap));  // gath_cap
   uint32_t* gw1 = gw0 + p.gath_cap;                                             // gath_cap
-  uint32_t* hist = gw1 + p.gath_cap;                                            // 2 x kRadix
-  uint32_t* hsum = hist + 2 * kRadix;                                           // kRadix
-  uint32_t* misc = hsum + kRadix;                                               // kMiscTotal
+  uint32_t* hist = gw1 + p.gath_cap;                                            // kHistWords
+  uint32_t* hloc = hist + 4 * kRadix;                                           // local levels
+  uint32_t* misc = hist + kHistWords;                                           // kMiscTotal
   uint32_t* bc = misc + kBc;
-  uint32_t* xchg = misc + kXchg;
   uint32_t* wtot = misc + kWtot;
+  const ClusterLevels CL{hist, misc + kOvw, bc};
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -483,9 +527,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   const int se = min(sb + segm, G);
   uint16_t* wlist = list + warp * segm;
   uint4* wvec = lvec + warp * p.lvec_cap;
-  const int wcap = p.cand_cap / kWarps;
-  uint32_t* wc0 = cw0 + warp * wcap;
-  uint32_t* wc1 = cw1 + warp * wcap;
+  uint8_t* wmask = lmask + warp * p.lvec_cap;
   // granules whose vectors all lie inside [0, len) (gv == 1: full vectors)
   const int Gf = gv == 1 ? static_cast<int>(min(v1, max(v0, p.len / VEC)) - v0) : G;
 
@@ -505,6 +547,17 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     cp_async_commit();
   };
   if (nstage > 0 && blockIdx.x / S < p.batch) prefetch(blockIdx.x / S);
+  // receive histograms and cluster-pushed words start cleared in every CTA
+  if (tid < kRadix) {
+    hist[kRadix + tid] = 0;
+    hist[2 * kRadix + tid] = 0;
+    hist[3 * kRadix + tid] = 0;
+  }
+  if (tid < 4) misc[kOvw + tid] = 0;
+  if (tid < 4) misc[kXmax + tid] = 0;
+  int lvl = 0;  // cluster levels so far (runs across rows; identical in the cluster)
+  if constexpr (S > 1) cg::this_cluster().sync();
+  else __syncthreads();
 
 #pragma unroll 1
   for (int64_t row = blockIdx.x / S; row < p.batch; row += row_step) {
@@ -524,7 +577,6 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     uint32_t t16 = 0;
     int lc = 0;  // granules in this warp's list (warp-uniform)
     bool vec_kept = false;  // the list's vectors were copied to wvec by the streaming pass
-    int lvl = 0;
     bool guess_mode = have_guess;
 #pragma unroll 1
     for (int attempt = 0; attempt < 2; ++attempt) {
@@ -619,9 +671,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         uint32_t total = 0;
         for (int w = 0; w < kWarps; ++w) total += misc[kLcnt + w];
         if constexpr (S > 1) {
-          if (tid == 0) xchg[2] = total;
+          if (tid < S) dsmem_red_add_u32(misc + kXtot, static_cast<uint32_t>(tid), total);
           cg::this_cluster().sync();
-          total = cluster_sum<S>(xchg + 2);
+          total = misc[kXtot];
         }
         t16 = t_guess;
         __syncthreads();  // every warp has read the per-warp counts before they change
@@ -640,96 +692,158 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       if (p.g_total >= static_cast<int64_t>(k)) {
         // histogram over the 256 key values just below the row's largest maximum
         if constexpr (S > 1) {
-          if (tid == 0) xchg[3] = mmax;
+          if (tid < S) dsmem_red_max_u32(misc + kXmax, static_cast<uint32_t>(tid), mmax);
           cg::this_cluster().sync();
-#pragma unroll 1
-          for (int r = 0; r < S; ++r) mmax = max(mmax, dsmem_ld_u32(xchg + 3, static_cast<uint32_t>(r)));
+          mmax = misc[kXmax];
         }
         const uint32_t wbase = mmax > 255u ? mmax - 255u : 0u;
-        uint32_t* h = hist + (lvl & 1) * kRadix;
-        uint32_t* ov = misc + kOver + (lvl & 1);
-        if (tid < kRadix) h[tid] = 0;
-        if (tid == 0) *ov = 0;
-        __syncthreads();
-        for (int g = sb + lane; g < se; g += 32) {
-          const uint32_t m = M[g];
-          hist_add(h, m - wbase, m >= wbase);
+        CL.begin();
+        for (int b0 = sb; b0 < se; b0 += 256) {  // 8 maxima per lane per step
+          const int base = b0 + lane * 8;
+          if (base < se) {
+            uint32_t m[8];
+            load_m8(M, base, m);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) hist_add(CL.loc(), m[e] - wbase, base + e < se && m[e] >= wbase);
+          }
         }
-        const LevelResult r = finish_level<S>(h, ov, hsum, bc, k);
-        ++lvl;
+        const LevelResult r = CL.finish<S>(lvl++, k);
         if (r.found) {
           t16 = wbase + r.digit;
         } else {
           // fewer than k maxima within 256 keys of the largest: two 8-bit levels
-          h = hist + (lvl & 1) * kRadix;
-          ov = misc + kOver + (lvl & 1);
-          if (tid < kRadix) h[tid] = 0;
-          if (tid == 0) *ov = 0;
-          __syncthreads();
-          for (int g = sb + lane; g < se; g += 32) hist_add(h, M[g] >> 8, true);
-          const LevelResult r1 = finish_level<S>(h, ov, hsum, bc, k);
-          ++lvl;
-          h = hist + (lvl & 1) * kRadix;
-          ov = misc + kOver + (lvl & 1);
-          if (tid < kRadix) h[tid] = 0;
-          if (tid == 0) *ov = 0;
-          __syncthreads();
-          for (int g = sb + lane; g < se; g += 32) {
-            const uint32_t m = M[g];
-            hist_add(h, m & 0xFFu, (m >> 8) == r1.digit);
+          CL.begin();
+          for (int b0 = sb; b0 < se; b0 += 256) {
+            const int base = b0 + lane * 8;
+            if (base < se) {
+              uint32_t m[8];
+              load_m8(M, base, m);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) hist_add(CL.loc(), m[e] >> 8, base + e < se);
+            }
           }
-          const LevelResult r2 = finish_level<S>(h, ov, hsum, bc, k - r1.above);
-          ++lvl;
+          const LevelResult r1 = CL.finish<S>(lvl++, k);
+          CL.begin();
+          for (int b0 = sb; b0 < se; b0 += 256) {
+            const int base = b0 + lane * 8;
+            if (base < se) {
+              uint32_t m[8];
+              load_m8(M, base, m);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                hist_add(CL.loc(), m[e] & 0xFFu, base + e < se && (m[e] >> 8) == r1.digit);
+            }
+          }
+          const LevelResult r2 = CL.finish<S>(lvl++, k - r1.above);
           t16 = (r1.digit << 8) | r2.digit;
         }
         t_guess = t16 > 0x0080u + kGuessMargin ? t16 - kGuessMargin : 0u;
         have_guess = true;
       }
       // this warp's list: granules whose maximum reaches t16, in index order
+      // (8 consecutive maxima per lane per step, lanes in order)
       lc = 0;
-      for (int i0 = sb; i0 < se; i0 += 32) {
-        const int g = i0 + lane;
-        const bool pass = g < se && M[g] >= t16;
-        const uint32_t b = __ballot_sync(kFull, pass);
-        if (pass) wlist[lc + __popc(b & lt_mask)] = static_cast<uint16_t>(g);
-        lc += __popc(b);
+      for (int b0 = sb; b0 < se; b0 += 256) {
+        const int base = b0 + lane * 8;
+        uint32_t mask = 0;
+        if (base < se) {
+          uint32_t m[8];
+          load_m8(M, base, m);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mask |= static_cast<uint32_t>(base + e < se && m[e] >= t16) << e;
+        }
+        const uint32_t c = __popc(mask);
+        int pos = lc + static_cast<int>(warp_excl_scan(c));
+        lc += static_cast<int>(warp_sum(c));
+        while (mask) {
+          const int e = __ffs(mask) - 1;
+          mask &= mask - 1;
+          wlist[pos++] = static_cast<uint16_t>(base + e);
+        }
       }
       __syncwarp();  // the warp's list is read back by other lanes below
       break;
     }
 
     // ---- D: candidates (key >= t, or NaN) of the listed granules, in index order ----
-    // With one vector per granule the listed vectors sit in the warp's shared
-    // copy (kept by the streaming pass, or fetched now from L2); each lane takes
-    // one granule, and positions come from ballots (almost every listed granule
-    // holds exactly one candidate).
+    // Pass 1 counts each warp's candidates (keeping every listed vector's 8-bit
+    // candidate mask); a prefix over the warps then gives each warp its place in
+    // the CTA's candidate array, and pass 2 writes them there. Listed vectors are
+    // read from the warp's shared copy (kept by the streaming pass, or fetched
+    // now from L2); entries beyond its capacity are read from L2 in both passes.
     const uint32_t T_full = (KB == 16) ? t16 : (t16 << 16);
     const float tval = key_threshold_value<ES>(T_full);
-    int cc = 0;  // this warp's candidates (may exceed wcap: then only counted)
     const uint4* slice = rowv + v0;
     const int nvs = static_cast<int>(nv);  // vectors in this slice
     const int nfull = gv == 1 ? Gf : static_cast<int>(max(int64_t(0), min(nv, p.len / VEC - v0)));
-    if (gv == 1 && lc <= p.lvec_cap) {
-      if (!vec_kept) {  // fetch the listed vectors into the warp's shared copy
-        for (int j = lane; j < lc; j += 32) {
-          const int v = wlist[j];
-          wvec[j] = v < nfull ? ld_nc_v4(slice + v) : load_vec<ES>(rowp, v0 + v, p.len);
-        }
-        __syncwarp();
+    // candidate mask of slice vector v (ragged last vector: lanes past len cleared)
+    auto vmask_of = [&](int v, const uint4& w) -> uint32_t {
+      uint32_t m = cand_mask<ES>(w, tval);
+      if (v >= nfull) {
+        const int64_t valid = p.len - (v0 + v) * VEC;
+        m &= valid <= 0 ? 0u : (valid >= VEC ? 0xFFu : ((1u << valid) - 1u));
       }
+      return m;
+    };
+    auto load_slice = [&](int v) -> uint4 {
+      return v < nfull ? ld_nc_v4(slice + v) : load_vec<ES>(rowp, v0 + v, p.len);
+    };
+    const int ncache = gv == 1 ? min(lc, p.lvec_cap) : 0;  // list entries held in wvec
+    if (gv == 1 && !vec_kept) {
+      for (int j = lane; j < ncache; j += 32) wvec[j] = load_slice(wlist[j]);
+      __syncwarp();
+    }
+    uint32_t wc = 0;
+    for (int j = lane; j < lc; j += 32) {
+      if (gv == 1) {
+        const int v = wlist[j];
+        const uint32_t m = vmask_of(v, j < ncache ? wvec[j] : load_slice(v));
+        if (j < ncache) wmask[j] = static_cast<uint8_t>(m);
+        wc += __popc(m);
+      } else {
+        const int vb = static_cast<int>(wlist[j]) * gv;
+        const int ve = min(vb + gv, nvs);
+        for (int v = vb; v < ve; ++v) wc += __popc(vmask_of(v, load_slice(v)));
+      }
+    }
+    wc = warp_sum(wc);
+    if (lane == 0) {
+      wtot[kWarps + warp] = wc;
+      misc[kLcnt + warp] = static_cast<uint32_t>(lc);
+    }
+    __syncthreads();
+    uint32_t cbase = 0, ncand = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const uint32_t t = wtot[kWarps + w];
+      if (w < warp) cbase += t;
+      ncand += t;
+    }
+    const bool cta_over = ncand > static_cast<uint32_t>(p.cand_cap);
+    if (!cta_over) {
+      // pass 2: write, lanes in index order; positions from ballots (almost every
+      // listed granule holds exactly one candidate)
       for (int j0 = 0; j0 < lc; j0 += 32) {
         const int j = j0 + lane;
-        uint32_t m = 0;
-        int v = 0;
+        int vb = 0, ve = 0;
+        uint32_t c = 0, m0 = 0;
+        uint4 w0 = make_uint4(0u, 0u, 0u, 0u);
         if (j < lc) {
-          v = wlist[j];
-          m = cand_mask<ES>(wvec[j], tval);
-          if (v >= nfull) {  // ragged last vector of the row
-            const int64_t valid = p.len - (v0 + v) * VEC;
-            m &= valid >= VEC ? 0xFFu : ((1u << valid) - 1u);
+          if (gv == 1) {
+            vb = wlist[j];
+            ve = vb + 1;
+            if (j < ncache) {
+              m0 = wmask[j];
+            } else {
+              w0 = load_slice(vb);
+              m0 = vmask_of(vb, w0);
+            }
+            c = __popc(m0);
+          } else {
+            vb = static_cast<int>(wlist[j]) * gv;
+            ve = min(vb + gv, nvs);
+            for (int v = vb; v < ve; ++v) c += __popc(vmask_of(v, load_slice(v)));
           }
         }
-        const uint32_t c = __popc(m);
         int excl = 0, tot = 0;
 #pragma unroll 1
         for (uint32_t t = 1;; ++t) {
@@ -738,102 +852,71 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           excl += __popc(b & lt_mask);
           tot += __popc(b);
         }
-        int pos = cc + excl;
-        cc += tot;
-        const uint32_t ibase = static_cast<uint32_t>((v0 + v) * VEC);
-        while (m) {
-          const int e = __ffs(m) - 1;
-          m &= m - 1;
-          if (pos < wcap) {
-            uint32_t bits;
-            if constexpr (ES == 2) bits = reinterpret_cast<const uint16_t*>(wvec + j)[e];
-            else bits = reinterpret_cast<const uint32_t*>(wvec + j)[e];
-            wc0[pos] = cand_pack<ES>(bits);
-            wc1[pos] = ibase + e;
-          }
-          ++pos;
-        }
-      }
-    } else {
-      // several vectors per granule: count the granule's candidates, then write
-      // them (vectors re-read), so each lane's output stays in index order
-      auto vec_mask = [&](int v, uint4& w) -> uint32_t {
-        w = v < nfull ? ld_nc_v4(slice + v) : load_vec<ES>(rowp, v0 + v, p.len);
-        uint32_t m = cand_mask<ES>(w, tval);
-        if (v >= nfull) {
-          const int64_t valid = p.len - (v0 + v) * VEC;
-          m &= valid <= 0 ? 0u : (valid >= VEC ? 0xFFu : ((1u << valid) - 1u));
-        }
-        return m;
-      };
-      for (int j0 = 0; j0 < lc; j0 += 32) {
-        const int j = j0 + lane;
-        uint32_t c = 0;
-        int vb = 0, ve = 0;
-        if (j < lc) {
-          vb = static_cast<int>(wlist[j]) * gv;
-          ve = min(vb + gv, nvs);
-          for (int v = vb; v < ve; ++v) {
-            uint4 w;
-            c += __popc(vec_mask(v, w));
-          }
-        }
-        int pos = cc + static_cast<int>(warp_excl_scan(c));
-        cc += static_cast<int>(warp_sum(c));
+        uint32_t pos = cbase + excl;
+        cbase += tot;
         if (c == 0) continue;
         for (int v = vb; v < ve; ++v) {
           uint4 w;
-          const uint32_t m = vec_mask(v, w);
+          uint32_t m;
+          const bool in_cache = gv == 1 && j < ncache;
+          if (gv == 1) {
+            w = w0;
+            m = m0;
+          } else {
+            w = load_slice(v);
+            m = vmask_of(v, w);
+          }
           const uint32_t ibase = static_cast<uint32_t>((v0 + v) * VEC);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            if ((m >> e) & 1u) {
-              if (pos < wcap) {
-                wc0[pos] = cand_pack<ES>(elem_bits<ES>(w, e));
-                wc1[pos] = ibase + e;
-              }
-              ++pos;
+          while (m) {
+            const int e = __ffs(m) - 1;
+            m &= m - 1;
+            uint32_t bits;
+            if (in_cache) {
+              if constexpr (ES == 2) bits = reinterpret_cast<const uint16_t*>(wvec + j)[e];
+              else bits = reinterpret_cast<const uint32_t*>(wvec + j)[e];
+            } else {
+              bits = elem_bits<ES>(w, e);
             }
+            cw0[pos] = cand_pack<ES>(bits);
+            cw1[pos] = ibase + e;
+            ++pos;
           }
         }
       }
     }
+    // candidates are contiguous in index order: 8 equal warp segments for B and C
     if (lane == 0) {
-      misc[kSegBase + warp] = static_cast<uint32_t>(warp * wcap);
-      misc[kSegCnt + warp] = static_cast<uint32_t>(min(cc, wcap));
-      wtot[kWarps + warp] = static_cast<uint32_t>(cc);
-      misc[kLcnt + warp] = static_cast<uint32_t>(lc);
+      const uint32_t per = (ncand + kWarps - 1) / kWarps;
+      const uint32_t b = min(static_cast<uint32_t>(warp) * per, ncand);
+      misc[kSegBase + warp] = b;
+      misc[kSegCnt + warp] = min(b + per, ncand) - b;
     }
-    const bool cta_over = __syncthreads_or(cc > wcap) != 0;
+    __syncthreads();
 
     // ---- cluster: ship every CTA's candidates to the leader (rank 0) --------------
     bool dense = !cta_over;
     bool work_here = true;  // this CTA runs the selection (always, unless a non-leader)
     if constexpr (S > 1) {
-      if (tid < kWarps) misc[kPub + tid] = wtot[kWarps + tid];
-      if (tid == 0) misc[kPub + kWarps] = cta_over ? 1u : 0u;
-      cg::this_cluster().sync();
-      if (tid < S * (kWarps + 1)) {
-        const int r = tid / (kWarps + 1), j = tid - r * (kWarps + 1);
-        misc[kAll + tid] = dsmem_ld_u32(misc + kPub + j, static_cast<uint32_t>(r));
+      if (tid == 0) {
+        misc[kPub] = ncand;
+        misc[kPub + 1] = cta_over ? 1u : 0u;
       }
+      cg::this_cluster().sync();
+      if (tid < 2 * S) misc[kAll + tid] = dsmem_ld_u32(misc + kPub + (tid & 1), static_cast<uint32_t>(tid >> 1));
       __syncthreads();
       uint32_t total = 0, before = 0;
       bool any_over = false;
       for (int r = 0; r < S; ++r) {
-        any_over |= misc[kAll + r * (kWarps + 1) + kWarps] != 0u;
-        for (int w = 0; w < kWarps; ++w) {
-          const uint32_t c = misc[kAll + r * (kWarps + 1) + w];
-          if (r < rank || (r == rank && w < warp)) before += c;
-          total += c;
-        }
+        any_over |= misc[kAll + 2 * r + 1] != 0u;
+        const uint32_t c = misc[kAll + 2 * r];
+        if (r < rank) before += c;
+        total += c;
       }
       dense = !any_over && total <= static_cast<uint32_t>(p.gath_cap);
       if (dense) {
-        const int mine = min(cc, wcap);
-        for (int c = lane; c < mine; c += 32) {
-          dsmem_st_u32(gw0 + before + c, 0u, wc0[c]);
-          dsmem_st_u32(gw1 + before + c, 0u, wc1[c]);
+        for (uint32_t c = tid; c < ncand; c += kThreads) {
+          dsmem_st_u32(gw0 + before + c, 0u, cw0[c]);
+          dsmem_st_u32(gw1 + before + c, 0u, cw1[c]);
         }
         cg::this_cluster().sync();  // the leader's gathered array is complete
         work_here = rank == 0;
@@ -856,14 +939,13 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       const uint32_t* c1 = (S > 1) ? gw1 : cw1;
       const int sbase = static_cast<int>(misc[kSegBase + warp]);
       const int scnt = static_cast<int>(misc[kSegCnt + warp]);
-      uint32_t need = k, kstar = 0;
+      uint32_t need = k, kstar = 0, small = 0;
       uint32_t wbase = t16;
+      uint32_t* ovl = misc + kOvl;
 #pragma unroll 1
       while (true) {  // windowed level on the top 16 key bits, moving up from t16
-        uint32_t* h = hist + (lvl & 1) * kRadix;
-        uint32_t* ov = misc + kOver + (lvl & 1);
-        if (tid < kRadix) h[tid] = 0;
-        if (tid == 0) *ov = 0;
+        if (tid < kRadix) hloc[tid] = 0;
+        if (tid == 0) *ovl = 0;
         __syncthreads();
         uint32_t lover = 0;
         for (int c = lane; c < round_up32(scnt); c += 32) {
@@ -871,38 +953,67 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           const uint32_t k16v = cand_key<ES>(okc ? c0[sbase + c] : 0u) >> (KB - 16);
           const bool ok = okc && k16v >= wbase;
           const uint32_t d = k16v - wbase;
-          hist_add(h, d, ok && d < 256u);
+          hist_add(hloc, d, ok && d < 256u);
           lover += __popc(__ballot_sync(kFull, ok && d >= 256u));
         }
-        if (lane == 0 && lover) atomicAdd(ov, lover);
-        const LevelResult r = finish_level<1>(h, ov, hsum, bc, need);
-        ++lvl;
+        if (lane == 0 && lover) atomicAdd(ovl, lover);
+        __syncthreads();
+        const LevelResult r = scan_level(hloc, *ovl, bc, need);
         if (r.shift && wbase + 256u <= 0xFFFFu) {
           wbase += 256u;
           continue;
         }
         kstar = (wbase + r.digit) << (KB - 16);
         need -= r.above;
+        small = r.count;
         break;
       }
       if constexpr (KB == 32) {
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {  // low 16 bits: two 8-bit levels
-          const int shift = 8 - 8 * j;
-          uint32_t* h = hist + (lvl & 1) * kRadix;
-          uint32_t* ov = misc + kOver + (lvl & 1);
-          if (tid < kRadix) h[tid] = 0;
-          if (tid == 0) *ov = 0;
+        const uint32_t pre16 = kstar >> 16;
+        if (small <= 32) {
+          // few candidates share K*'s top 16 bits: collect them, then one warp
+          // ranks them exactly (the need-th largest of at most 32 keys)
+          if (tid == 0) *ovl = 0;
           __syncthreads();
-          const uint32_t pre = kstar >> (shift + 8);
           for (int c = lane; c < scnt; c += 32) {
             const uint32_t key = cand_key<ES>(c0[sbase + c]);
-            hist_add(h, (key >> shift) & 0xFFu, (key >> (shift + 8)) == pre);
+            if ((key >> 16) == pre16) hloc[atomicAdd(ovl, 1u)] = key;
           }
-          const LevelResult r = finish_level<1>(h, ov, hsum, bc, need);
-          ++lvl;
-          kstar |= r.digit << shift;
-          need -= r.above;
+          __syncthreads();
+          if (tid < 32) {
+            const uint32_t m = *ovl;
+            const uint32_t mine = lane < static_cast<int>(m) ? hloc[lane] : 0u;
+            uint32_t gt = 0, eq = 0;
+            for (uint32_t j = 0; j < m; ++j) {
+              const uint32_t other = __shfl_sync(0xFFFFFFFFu, mine, static_cast<int>(j));
+              gt += other > mine;
+              eq += other == mine;
+            }
+            if (lane < static_cast<int>(m) && gt < need && need <= gt + eq) {
+              bc[0] = mine;  // every lane holding K* writes the same values
+              bc[1] = gt;
+            }
+          }
+          __syncthreads();
+          kstar = bc[0];
+          need -= bc[1];
+          __syncthreads();
+        } else {
+#pragma unroll 1
+          for (int j = 0; j < 2; ++j) {  // low 16 bits: two 8-bit levels
+            const int shift = 8 - 8 * j;
+            if (tid < kRadix) hloc[tid] = 0;
+            __syncthreads();
+            const uint32_t pre = kstar >> (shift + 8);
+            for (int c = lane; c < scnt; c += 32) {
+              const uint32_t key = cand_key<ES>(c0[sbase + c]);
+              hist_add(hloc, (key >> shift) & 0xFFu, (key >> (shift + 8)) == pre);
+            }
+            __syncthreads();
+            const LevelResult r = scan_level(hloc, 0u, bc, need);
+            kstar |= r.digit << shift;
+            need -= r.above;
+          }
         }
       }
       const uint32_t r_ties = need;  // elements equal to K* that are taken
@@ -966,11 +1077,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       uint32_t wbase = t16;
 #pragma unroll 1
       while (true) {
-        uint32_t* h = hist + (lvl & 1) * kRadix;
-        uint32_t* ov = misc + kOver + (lvl & 1);
-        if (tid < kRadix) h[tid] = 0;
-        if (tid == 0) *ov = 0;
-        __syncthreads();
+        CL.begin();
+        uint32_t* h = CL.loc();
         uint32_t lover = 0;
         visit([&](uint32_t key, bool ok) {
           const uint32_t k16v = key >> (KB - 16);
@@ -979,9 +1087,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           hist_add(h, d, ok && d < 256u);
           lover += __popc(__ballot_sync(kFull, ok && d >= 256u));
         });
-        if (lane == 0 && lover) atomicAdd(ov, lover);
-        const LevelResult r = finish_level<S>(h, ov, hsum, bc, need);
-        ++lvl;
+        if (lane == 0 && lover) atomicAdd(CL.ov(), lover);
+        const LevelResult r = CL.finish<S>(lvl++, need);
         if (r.shift && wbase + 256u <= 0xFFFFu) {
           wbase += 256u;
           continue;
@@ -994,17 +1101,13 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 #pragma unroll 1
         for (int j = 0; j < 2; ++j) {
           const int shift = 8 - 8 * j;
-          uint32_t* h = hist + (lvl & 1) * kRadix;
-          uint32_t* ov = misc + kOver + (lvl & 1);
-          if (tid < kRadix) h[tid] = 0;
-          if (tid == 0) *ov = 0;
-          __syncthreads();
+          CL.begin();
+          uint32_t* h = CL.loc();
           const uint32_t pre = kstar >> (shift + 8);
           visit([&](uint32_t key, bool ok) {
             hist_add(h, (key >> shift) & 0xFFu, ok && (key >> (shift + 8)) == pre);
           });
-          const LevelResult r = finish_level<S>(h, ov, hsum, bc, need);
-          ++lvl;
+          const LevelResult r = CL.finish<S>(lvl++, need);
           kstar |= r.digit << shift;
           need -= r.above;
         }
@@ -1032,16 +1135,13 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         cta_eq += te;
       }
       if constexpr (S > 1) {
-        if (tid == 0) {
-          xchg[0] = cta_gt;
-          xchg[1] = cta_eq;
+        if (tid > rank && tid < S) {  // push this CTA's counts to every later rank
+          dsmem_red_add_u32(misc + kXpreGt, static_cast<uint32_t>(tid), cta_gt);
+          dsmem_red_add_u32(misc + kXpreEq, static_cast<uint32_t>(tid), cta_eq);
         }
         cg::this_cluster().sync();
-#pragma unroll 1
-        for (int r = 0; r < rank; ++r) {
-          base_gt += dsmem_ld_u32(xchg, static_cast<uint32_t>(r));
-          base_eq += dsmem_ld_u32(xchg + 1, static_cast<uint32_t>(r));
-        }
+        base_gt += misc[kXpreGt];
+        base_eq += misc[kXpreEq];
       }
       // write pass: one granule per lane, lanes in index order
       for (int j0 = 0; j0 < lc; j0 += 32) {
@@ -1090,8 +1190,11 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         }
       }
     }
-    // the next row reuses every shared buffer; cluster peers may still read ours
+    // the next row reuses every shared buffer; cluster peers may still read ours,
+    // and the words they push into must be clear before anyone starts the next row
     if constexpr (S > 1) {
+      __syncthreads();
+      if (tid < 4) misc[kXmax + tid] = 0;
       cg::this_cluster().sync();
     } else {
       __syncthreads();
