@@ -64,17 +64,31 @@ def measured_peak():
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary
-    of this workload, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    """DRAM bytes per launch of the dominant kernel, from the committed ncu summary
+    of this workload (a line `bench-traffic: workload=.. kernel_hash=..
+    dram_bytes_per_launch=..` in profiles/*.md), if it was taken on the current
+    kernel source; else None."""
+    pdir = os.path.join(ROOT, "profiles")
+    found = None
     try:
-        with open(path) as fh:
-            d = json.load(fh)
-    except (OSError, ValueError):
+        names = sorted(os.listdir(pdir))
+    except OSError:
         return None, None
-    if d.get("kernel_hash") != kernel_hash():
-        return None, "stale (kernel changed since the ncu capture)"
-    return d.get("dram_bytes_per_launch"), d.get("note")
+    for fn in names:
+        if not fn.endswith(".md"):
+            continue
+        with open(os.path.join(pdir, fn), encoding="utf-8") as fh:
+            for line in fh:
+                if line.startswith("bench-traffic:"):
+                    kv = dict(t.split("=", 1) for t in line.split()[1:] if "=" in t)
+                    if kv.get("workload") == workload:
+                        found = (kv, fn)
+    if found is None:
+        return None, None
+    kv, fn = found
+    if kv.get("kernel_hash") != kernel_hash():
+        return None, f"stale: {fn} was captured on kernel {kv.get('kernel_hash')}"
+    return int(kv["dram_bytes_per_launch"]), f"ncu capture summarised in profiles/{fn}"
 
 
 class ClockSampler:
@@ -374,6 +388,21 @@ def e2e_measure(w, dstk, dev, stream, steps):
             "ms_per_step": round(sec / steps * 1e3, 4)}
 
 
+def run_case(args, w):
+    """Profiling case (for ncu captures): generate the workload (first --rows rows)
+    on the GPU and call topk() --calls times. No timing, no JSON line."""
+    import sampler_topk_selection_ds_b300 as dstk
+    if args.rows:
+        w = w.scaled(args.rows)
+    x = workloads.generate(w, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(args.calls):
+        dstk.topk(x, w.k, sorted_index=w.sorted_index, return_value=w.return_value, nan_flag=flag)
+    torch.cuda.synchronize()
+    print(f"case {w.name}: {w.batch} rows x {w.length}, {args.calls} calls, nan_flag={int(flag.item())}")
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -384,8 +413,14 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", action="store_true",
+                    help="profiling case: run the workload --calls times, untimed (for ncu)")
+    ap.add_argument("--rows", type=int, default=0, help="--case: use only the first ROWS rows")
+    ap.add_argument("--calls", type=int, default=3, help="--case: number of calls")
     args = ap.parse_args(argv)
     w = workloads.WORKLOADS[args.workload]
+    if args.case:
+        return run_case(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -487,6 +487,13 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   constexpr uint32_t kFull = 0xFFFFFFFFu;
   using VT = typename std::conditional<ES == 2, uint16_t, uint32_t>::type;
 
+  // Programmatic dependent launch: a kernel queued behind this one may be
+  // scheduled now, and this one touches global memory only once every kernel
+  // queued before it has completed (griddepcontrol.wait), so its inputs and
+  // outputs are ordered as in a plain stream whatever those kernels do.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // next-row prefetch: slot (i, thread) holds step i of the thread's P1 vectors
   uint4* stage = reinterpret_cast<uint4*>(smem_raw);                            // stage_vecs*kThreads
