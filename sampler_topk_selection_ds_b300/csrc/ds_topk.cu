@@ -168,27 +168,33 @@ DeviceInfo g_dev[kMaxDevices];
 
 constexpr int kMaxSmem = static_cast<int>(kSmemLimit);
 
-template <int ES, int S>
+template <int ES, int S, bool GV1>
 cudaError_t prepare_kernel() {
-  auto* fn = ds_topk_dev::topk_rows_kernel<ES, S>;
+  auto* fn = ds_topk_dev::topk_rows_kernel<ES, S, GV1>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
   if (e != cudaSuccess) return e;
   if (S > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
 }
 
+template <int ES, bool GV1>
+cudaError_t prepare_variant() {
+  cudaError_t e;
+  if ((e = prepare_kernel<ES, 1, GV1>()) != cudaSuccess) return e;
+  if ((e = prepare_kernel<ES, 2, GV1>()) != cudaSuccess) return e;
+  if ((e = prepare_kernel<ES, 4, GV1>()) != cudaSuccess) return e;
+  if ((e = prepare_kernel<ES, 8, GV1>()) != cudaSuccess) return e;
+  return prepare_kernel<ES, 16, GV1>();
+}
+
 template <int ES>
 cudaError_t prepare_dtype() {
-  cudaError_t e;
-  if ((e = prepare_kernel<ES, 1>()) != cudaSuccess) return e;
-  if ((e = prepare_kernel<ES, 2>()) != cudaSuccess) return e;
-  if ((e = prepare_kernel<ES, 4>()) != cudaSuccess) return e;
-  if ((e = prepare_kernel<ES, 8>()) != cudaSuccess) return e;
-  return prepare_kernel<ES, 16>();
+  const cudaError_t e = prepare_variant<ES, true>();
+  return e != cudaSuccess ? e : prepare_variant<ES, false>();
 }
 
 // Largest cluster size (<= 16) that can be resident with the biggest CTA we launch.
-template <int ES>
+template <int ES, bool GV1>
 int probe_cluster16() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(16, 1, 1);
@@ -202,7 +208,7 @@ int probe_cluster16() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, ds_topk_dev::topk_rows_kernel<ES, 16>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, ds_topk_dev::topk_rows_kernel<ES, 16, GV1>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -219,9 +225,10 @@ int device_info(DeviceInfo* out) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
       return DS_TOPK_ECUDA;
     if (prepare_dtype<2>() != cudaSuccess || prepare_dtype<4>() != cudaSuccess) return DS_TOPK_ECUDA;
-    const int c16 = (probe_cluster16<2>() > 0 && probe_cluster16<4>() > 0) ? 16 : 8;
+    const bool ok16 = probe_cluster16<2, true>() > 0 && probe_cluster16<4, true>() > 0 &&
+                      probe_cluster16<2, false>() > 0 && probe_cluster16<4, false>() > 0;
     d.sm_count = sms;
-    d.max_cluster = c16;
+    d.max_cluster = ok16 ? 16 : 8;
     d.ready = true;
   }
   *out = d;
@@ -230,9 +237,9 @@ int device_info(DeviceInfo* out) {
 
 // How many clusters of S CTAs (S = 1: plain CTAs) of this kernel can be resident
 // at once with `smem` bytes of dynamic shared memory each.
-template <int ES, int S>
+template <int ES, int S, bool GV1>
 int resident_clusters(int smem, int sm_count) {
-  auto* fn = ds_topk_dev::topk_rows_kernel<ES, S>;
+  auto* fn = ds_topk_dev::topk_rows_kernel<ES, S, GV1>;
   int n = 0;
   if (S == 1) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess) {
@@ -259,33 +266,41 @@ int resident_clusters(int smem, int sm_count) {
   return n;
 }
 
+template <int ES, bool GV1>
+int resident_variant(int S, int smem, int sm_count) {
+  switch (S) {
+    case 1: return resident_clusters<ES, 1, GV1>(smem, sm_count);
+    case 2: return resident_clusters<ES, 2, GV1>(smem, sm_count);
+    case 4: return resident_clusters<ES, 4, GV1>(smem, sm_count);
+    case 8: return resident_clusters<ES, 8, GV1>(smem, sm_count);
+    default: return resident_clusters<ES, 16, GV1>(smem, sm_count);
+  }
+}
+
 struct ResidencyEntry {
-  int dev, es, S, smem, clusters;
+  int dev, es, S, gv1, smem, clusters;
 };
 constexpr int kResidencySlots = 64;
 ResidencyEntry g_residency[kResidencySlots];
 int g_residency_used = 0;
 
-// Cached resident_clusters() per (device, dtype, cluster size, shared memory).
-int resident_cached(int dev, int es, int S, int smem, int sm_count) {
+// Cached resident_clusters() per (device, dtype, cluster size, variant, shared memory).
+int resident_cached(int dev, const Plan& pl, int sm_count) {
+  const int es = pl.es, S = pl.pub.cluster_size, smem = pl.pub.smem_bytes;
+  const int gv1 = pl.prm.gv == 1 ? 1 : 0;
   std::lock_guard<std::mutex> lock(g_mu);
   for (int i = 0; i < g_residency_used; ++i) {
     const ResidencyEntry& e = g_residency[i];
-    if (e.dev == dev && e.es == es && e.S == S && e.smem == smem) return e.clusters;
+    if (e.dev == dev && e.es == es && e.S == S && e.gv1 == gv1 && e.smem == smem) return e.clusters;
   }
-  int n = 0;
-  switch (S) {
-    case 1: n = es == 2 ? resident_clusters<2, 1>(smem, sm_count) : resident_clusters<4, 1>(smem, sm_count); break;
-    case 2: n = es == 2 ? resident_clusters<2, 2>(smem, sm_count) : resident_clusters<4, 2>(smem, sm_count); break;
-    case 4: n = es == 2 ? resident_clusters<2, 4>(smem, sm_count) : resident_clusters<4, 4>(smem, sm_count); break;
-    case 8: n = es == 2 ? resident_clusters<2, 8>(smem, sm_count) : resident_clusters<4, 8>(smem, sm_count); break;
-    default: n = es == 2 ? resident_clusters<2, 16>(smem, sm_count) : resident_clusters<4, 16>(smem, sm_count); break;
-  }
-  if (g_residency_used < kResidencySlots) g_residency[g_residency_used++] = {dev, es, S, smem, n};
+  int n;
+  if (es == 2) n = gv1 ? resident_variant<2, true>(S, smem, sm_count) : resident_variant<2, false>(S, smem, sm_count);
+  else n = gv1 ? resident_variant<4, true>(S, smem, sm_count) : resident_variant<4, false>(S, smem, sm_count);
+  if (g_residency_used < kResidencySlots) g_residency[g_residency_used++] = {dev, es, S, gv1, smem, n};
   return n;
 }
 
-template <int ES, int S>
+template <int ES, int S, bool GV1>
 cudaError_t launch_one(const Plan& pl, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pl.pub.grid_ctas), 1, 1);
@@ -308,19 +323,24 @@ cudaError_t launch_one(const Plan& pl, cudaStream_t stream) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, ds_topk_dev::topk_rows_kernel<ES, S>, pl.prm);
+  return cudaLaunchKernelEx(&cfg, ds_topk_dev::topk_rows_kernel<ES, S, GV1>, pl.prm);
+}
+
+template <int ES, bool GV1>
+cudaError_t launch_variant(const Plan& pl, cudaStream_t stream) {
+  switch (pl.pub.cluster_size) {
+    case 1: return launch_one<ES, 1, GV1>(pl, stream);
+    case 2: return launch_one<ES, 2, GV1>(pl, stream);
+    case 4: return launch_one<ES, 4, GV1>(pl, stream);
+    case 8: return launch_one<ES, 8, GV1>(pl, stream);
+    case 16: return launch_one<ES, 16, GV1>(pl, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int ES>
 cudaError_t launch_dtype(const Plan& pl, cudaStream_t stream) {
-  switch (pl.pub.cluster_size) {
-    case 1: return launch_one<ES, 1>(pl, stream);
-    case 2: return launch_one<ES, 2>(pl, stream);
-    case 4: return launch_one<ES, 4>(pl, stream);
-    case 8: return launch_one<ES, 8>(pl, stream);
-    case 16: return launch_one<ES, 16>(pl, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return pl.prm.gv == 1 ? launch_variant<ES, true>(pl, stream) : launch_variant<ES, false>(pl, stream);
 }
 
 bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
@@ -351,13 +371,13 @@ extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int
   // persistent cluster walks several rows); otherwise without it.
   rc = make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, false, &pl);
   if (rc != DS_TOPK_OK) return rc;
-  int resident = resident_cached(dev_id, pl.es, pl.pub.cluster_size, pl.pub.smem_bytes, dev.sm_count);
+  int resident = resident_cached(dev_id, pl, dev.sm_count);
   if (resident > 0 && batch > resident) {
     Plan ps;
     if (make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, true, &ps) ==
             DS_TOPK_OK &&
         ps.prm.stage_vecs > 0) {
-      const int rs = resident_cached(dev_id, ps.es, ps.pub.cluster_size, ps.pub.smem_bytes, dev.sm_count);
+      const int rs = resident_cached(dev_id, ps, dev.sm_count);
       if (rs > 0 && batch > rs) {
         pl = ps;
         resident = rs;

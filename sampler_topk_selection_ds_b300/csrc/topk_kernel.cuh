@@ -293,10 +293,12 @@ __device__ __forceinline__ LevelResult scan_level(const uint32_t* h, uint32_t ov
   return r;
 }
 
-// Histogram levels whose counts are summed over the cluster, by reduce-scatter:
-// bin b belongs to CTA (b mod S); every CTA adds its local count of bin b into
-// the owner's receive histogram (red.shared::cluster, non-blocking), one cluster
-// barrier, then every CTA reads the 256 sums back from their owners (one
+// Histogram levels whose counts are summed over the cluster. Clusters of up to
+// 4 CTAs: every CTA adds its local counts into every CTA's receive histogram
+// (red.shared::cluster, non-blocking), one cluster barrier, local scan. Larger
+// clusters, by reduce-scatter: bin b belongs to CTA (b mod S); every CTA adds
+// its count of bin b into the owner's receive histogram, one cluster barrier,
+// then every CTA reads the 256 sums back from their owners (one
 // distributed-shared-memory load per thread) and scans them locally. Receive
 // histograms rotate over three buffers (the level counter runs on across rows,
 // identically in every CTA of the cluster): the buffer a level clears for the
@@ -321,7 +323,26 @@ struct ClusterLevels {
   __device__ LevelResult finish(int lvl, uint32_t need) const {
     __syncthreads();  // local counts complete
     const int tid = threadIdx.x;
-    if constexpr (S > 1) {
+    if constexpr (S > 1 && S <= 4) {
+      // small clusters: every CTA adds its counts into every CTA's receive
+      // histogram (S adds per bin), so no read-back round trip is needed
+      if (tid < kRadix) {
+        const uint32_t v = hist[tid];
+        if (v) {
+#pragma unroll
+          for (int r = 0; r < S; ++r) dsmem_red_add_u32(rcv(lvl) + tid, static_cast<uint32_t>(r), v);
+        }
+        rcv(lvl + 1)[tid] = 0;
+      }
+      if (tid == 0) {
+        if (ovw[0]) {
+          for (int r = 0; r < S; ++r) dsmem_red_add_u32(ovw + 1 + lvl % 3, static_cast<uint32_t>(r), ovw[0]);
+        }
+        ovw[1 + (lvl + 1) % 3] = 0;
+      }
+      cg::this_cluster().sync();
+      return scan_level(rcv(lvl), ovw[1 + lvl % 3], bc, need);
+    } else if constexpr (S > 4) {
       if (tid < kRadix) {
         const uint32_t v = hist[tid];
         if (v) dsmem_red_add_u32(rcv(lvl) + tid, static_cast<uint32_t>(tid % S), v);
@@ -432,18 +453,27 @@ __device__ __forceinline__ float max_value(uint32_t raw) {
 
 // Bit e set iff element e of the vector is a candidate: not below the
 // threshold value, or NaN (unordered comparison), so a granule whose maximum
-// reaches the threshold always contributes at least one candidate.
+// reaches the threshold always contributes at least one candidate. bf16 uses a
+// packed compare of both halves (setp.geu.bf16x2: exact for subnormals, the
+// first predicate reports the low half, i.e. the even element); tv2 holds the
+// threshold's bf16 bits in both halves.
 template <int ES>
-__device__ __forceinline__ uint32_t cand_mask(const uint4& w, float tval) {
+__device__ __forceinline__ uint32_t cand_mask(const uint4& w, float tval, uint32_t tv2) {
   uint32_t m = 0;
   if constexpr (ES == 2) {
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      m |= static_cast<uint32_t>(!(__uint_as_float(ws[j] << 16) < tval)) << (2 * j);
-      m |= static_cast<uint32_t>(!(__uint_as_float(ws[j] & 0xFFFF0000u) < tval)) << (2 * j + 1);
+      uint32_t r;
+      asm("{\n\t.reg .pred lo, hi;\n\t"
+          "setp.geu.bf16x2 lo|hi, %1, %2;\n\t"
+          "selp.u32 %0, 1, 0, lo;\n\t"
+          "@hi or.b32 %0, %0, 2;\n\t}"
+          : "=r"(r) : "r"(ws[j]), "r"(tv2));
+      m |= r << (2 * j);
     }
   } else {
+    (void)tv2;
     m = static_cast<uint32_t>(!(__uint_as_float(w.x) < tval)) |
         static_cast<uint32_t>(!(__uint_as_float(w.y) < tval)) << 1 |
         static_cast<uint32_t>(!(__uint_as_float(w.z) < tval)) << 2 |
@@ -479,7 +509,10 @@ __device__ __forceinline__ void load_m8(const uint16_t* M, int base, uint32_t m[
   m[6] = q.w & 0xFFFFu; m[7] = q.w >> 16;
 }
 
-template <int ES, int S>
+// GV1: one 16-byte vector per granule (every slice of at most 8192 vectors);
+// the general case (several vectors per granule, very long slices) is a
+// separate instantiation so that its code does not weigh on the common one.
+template <int ES, int S, bool GV1>
 __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) {
   using T = Traits<ES>;
   constexpr int VEC = T::kVec;
@@ -522,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   const int64_t v0 = rank * p.vec_per_cta;
   const int64_t v1 = min(v0 + p.vec_per_cta, p.nvec);
   const int64_t nv = v1 > v0 ? v1 - v0 : 0;
-  const int gv = p.gv;
+  const int gv = GV1 ? 1 : p.gv;
   const int G = static_cast<int>((nv + gv - 1) / gv);
   const uint32_t k = static_cast<uint32_t>(p.k);
   const int64_t row_step = gridDim.x / S;
@@ -760,8 +793,16 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           for (int e = 0; e < 8; ++e) mask |= static_cast<uint32_t>(base + e < se && m[e] >= t16) << e;
         }
         const uint32_t c = __popc(mask);
-        int pos = lc + static_cast<int>(warp_excl_scan(c));
-        lc += static_cast<int>(warp_sum(c));
+        int excl = 0, tot = 0;
+#pragma unroll 1
+        for (uint32_t t = 1;; ++t) {  // positions from ballots: counts are mostly 0 or 1
+          const uint32_t b = __ballot_sync(kFull, c >= t);
+          if (b == 0) break;
+          excl += __popc(b & lt_mask);
+          tot += __popc(b);
+        }
+        int pos = lc + excl;
+        lc += tot;
         while (mask) {
           const int e = __ffs(mask) - 1;
           mask &= mask - 1;
@@ -780,12 +821,13 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     // now from L2); entries beyond its capacity are read from L2 in both passes.
     const uint32_t T_full = (KB == 16) ? t16 : (t16 << 16);
     const float tval = key_threshold_value<ES>(T_full);
+    const uint32_t tv2 = (__float_as_uint(tval) >> 16) * 0x00010001u;  // bf16 bits, both halves
     const uint4* slice = rowv + v0;
     const int nvs = static_cast<int>(nv);  // vectors in this slice
     const int nfull = gv == 1 ? Gf : static_cast<int>(max(int64_t(0), min(nv, p.len / VEC - v0)));
     // candidate mask of slice vector v (ragged last vector: lanes past len cleared)
     auto vmask_of = [&](int v, const uint4& w) -> uint32_t {
-      uint32_t m = cand_mask<ES>(w, tval);
+      uint32_t m = cand_mask<ES>(w, tval, tv2);
       if (v >= nfull) {
         const int64_t valid = p.len - (v0 + v) * VEC;
         m &= valid <= 0 ? 0u : (valid >= VEC ? 0xFFu : ((1u << valid) - 1u));
