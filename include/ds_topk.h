@@ -125,8 +125,10 @@ DS_TOPK_API int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, in
 
 /* Which kernel family a call runs. */
 typedef enum {
-  DS_TOPK_PATH_ROW = 0,     /* one CTA per row                                     */
-  DS_TOPK_PATH_CLUSTER = 1  /* one thread-block cluster per row (row split in slices) */
+  DS_TOPK_PATH_ROW = 0,      /* one CTA per row                                     */
+  DS_TOPK_PATH_CLUSTER = 1,  /* one thread-block cluster per row (row split in slices) */
+  DS_TOPK_PATH_WARP_ROWS = 2 /* one warp per row, several rows per CTA: many rows of at
+                                most 65536 elements with k <= 1024                   */
 } ds_topk_path;
 
 /* Launch plan of one ds_topk call, as chosen by the host dispatcher. */
@@ -134,11 +136,16 @@ typedef struct {
   int32_t path;                /* ds_topk_path                                         */
   int32_t cluster_size;        /* CTAs cooperating on one row (1 for DS_TOPK_PATH_ROW) */
   int32_t threads_per_cta;
-  int32_t vectors_per_granule; /* 16-byte vectors summarised by one granule maximum     */
-  int64_t grid_ctas;           /* CTAs if every row had its own cluster; ds_topk launches
-                                  at most as many as can be co-resident, and each
-                                  persistent cluster then walks rows with a stride      */
-  int64_t granules_per_cta;    /* size of the per-CTA granule-maximum array            */
+  int32_t vectors_per_granule; /* 16-byte vectors summarised by one granule maximum
+                                  (1 on DS_TOPK_PATH_WARP_ROWS: vectors are tested one
+                                  by one)                                              */
+  int64_t grid_ctas;           /* CTAs if every row had its own cluster (warp rows: if
+                                  every 8 rows had their own CTA); ds_topk launches at
+                                  most as many as can be co-resident, and each
+                                  persistent cluster (warp) then walks rows with a
+                                  stride                                               */
+  int64_t granules_per_cta;    /* size of the per-CTA granule-maximum array; on
+                                  DS_TOPK_PATH_WARP_ROWS the candidate slots per warp  */
   int32_t smem_bytes;          /* dynamic shared memory per CTA                        */
   int32_t launches;            /* kernel launches per call                             */
 } ds_topk_plan_t;

@@ -25,6 +25,7 @@ FLAG_TIMEOUT = 2
 MAX_K = 4096
 PATH_ROW = 0
 PATH_CLUSTER = 1
+PATH_WARP_ROWS = 2
 
 
 class Plan(ctypes.Structure):

@@ -15,6 +15,7 @@
 
 #include "ds_topk.h"
 #include "topk_kernel.cuh"
+#include "warp_rows_kernel.cuh"
 
 namespace {
 
@@ -29,14 +30,22 @@ constexpr int kMaxCluster = 16;
 constexpr int64_t kSplitMinRowBytes = 64 * 1024;
 // A CTA of a split row gets at least this many bytes of it.
 constexpr int64_t kMinSliceBytes = 16 * 1024;
-// Dynamic shared memory one CTA may use (B300: 227 KB).
+// Dynamic shared memory one CTA may use (B300: 227 KB), shared memory of an SM
+// and the part of it the runtime reserves per resident CTA.
 constexpr int64_t kSmemLimit = 227 * 1024;
+constexpr int64_t kSmemPerSm = 228 * 1024;
+constexpr int64_t kSmemPerCtaReserved = 1024;
 // Most vectors per thread held in the next-row prefetch buffer.
 constexpr int64_t kMaxStageVecs = 16;
+// The one-warp-per-row path is taken from this many rows per SM on (below it a
+// whole CTA per row finishes a row sooner than a warp does).
+constexpr int64_t kWrMinRowsPerSm = 8;
 
 struct Plan {
   ds_topk_plan_t pub;
   Params prm;
+  ds_topk_dev::WrParams wprm;
+  bool warp_rows;
   int es;
 };
 
@@ -63,6 +72,59 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
   const int vec = 16 / es;
   const int64_t nvec = ceil_div(len, vec);
   const int64_t row_bytes = len * es;
+  out->warp_rows = false;
+
+  // Many short rows: one warp per row (candidate indices fit 16 bits, and a
+  // warp's candidate buffer of about 2k entries leaves room for 2+ CTAs per SM).
+  if (len <= ds_topk_dev::kWrMaxLen && k <= ds_topk_dev::kWrMaxK &&
+      batch >= kWrMinRowsPerSm * static_cast<int64_t>(sm_count)) {
+    int64_t cap = 2 * static_cast<int64_t>(k) + 256;
+    if (cap > static_cast<int64_t>(k) + 512) cap = static_cast<int64_t>(k) + 512;
+    cap = (cap + 31) / 32 * 32;
+    const int64_t all = (len + 31) / 32 * 32;  // every element fits
+    if (cap > all) cap = all;
+    // Most warps per SM first (3 CTAs, then 2), then the deepest streaming ring
+    // (3 chunks, then 2) that fits.
+    int depth = 0;
+    int64_t smem = 0;
+    for (int ctas = 3; ctas >= 2 && depth == 0; --ctas) {
+      for (int d = ds_topk_dev::kWrMaxDepth; d >= 2; --d) {
+        const int64_t b = ds_topk_dev::kWrWarps * ds_topk_dev::wr_warp_bytes(es, cap, d);
+        if (ctas * (b + kSmemPerCtaReserved) <= kSmemPerSm) {
+          depth = d;
+          smem = b;
+          break;
+        }
+      }
+    }
+    if (depth > 0) {
+      out->es = es;
+      out->warp_rows = true;
+      ds_topk_plan_t& pl = out->pub;
+      pl.path = DS_TOPK_PATH_WARP_ROWS;
+      pl.cluster_size = 1;
+      pl.threads_per_cta = ds_topk_dev::kWrThreads;
+      pl.vectors_per_granule = 1;
+      pl.grid_ctas = ceil_div(batch, ds_topk_dev::kWrWarps);
+      pl.granules_per_cta = cap;
+      pl.smem_bytes = static_cast<int32_t>(smem);
+      pl.launches = 1;
+      ds_topk_dev::WrParams& w = out->wprm;
+      w.x = nullptr;
+      w.batch = batch;
+      w.row_stride_bytes = row_stride * es;
+      w.len = static_cast<int32_t>(len);
+      w.nvec = static_cast<int32_t>(nvec);
+      w.cap = static_cast<int32_t>(cap);
+      w.depth = depth;
+      w.k = k;
+      w.return_value = 0;
+      w.out_values = nullptr;
+      w.out_indices = nullptr;
+      w.flag = nullptr;
+      return DS_TOPK_OK;
+    }
+  }
 
   int S = 1;
   if (row_bytes > kSplitMinRowBytes && batch < 2 * static_cast<int64_t>(sm_count)) {
@@ -189,8 +251,12 @@ cudaError_t prepare_variant() {
 
 template <int ES>
 cudaError_t prepare_dtype() {
-  const cudaError_t e = prepare_variant<ES, true>();
-  return e != cudaSuccess ? e : prepare_variant<ES, false>();
+  cudaError_t e = prepare_variant<ES, true>();
+  if (e == cudaSuccess) e = prepare_variant<ES, false>();
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ds_topk_dev::topk_warp_rows_kernel<ES>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+  return e;
 }
 
 // Largest cluster size (<= 16) that can be resident with the biggest CTA we launch.
@@ -284,17 +350,30 @@ constexpr int kResidencySlots = 64;
 ResidencyEntry g_residency[kResidencySlots];
 int g_residency_used = 0;
 
-// Cached resident_clusters() per (device, dtype, cluster size, variant, shared memory).
+template <int ES>
+int resident_warp_rows(int smem, int sm_count) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ds_topk_dev::topk_warp_rows_kernel<ES>,
+                                                    ds_topk_dev::kWrThreads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n * sm_count;
+}
+
+// Cached resident_clusters() per (device, dtype, cluster size, variant, shared memory);
+// the warp-rows kernel is cached as variant 2.
 int resident_cached(int dev, const Plan& pl, int sm_count) {
   const int es = pl.es, S = pl.pub.cluster_size, smem = pl.pub.smem_bytes;
-  const int gv1 = pl.prm.gv == 1 ? 1 : 0;
+  const int gv1 = pl.warp_rows ? 2 : (pl.prm.gv == 1 ? 1 : 0);
   std::lock_guard<std::mutex> lock(g_mu);
   for (int i = 0; i < g_residency_used; ++i) {
     const ResidencyEntry& e = g_residency[i];
     if (e.dev == dev && e.es == es && e.S == S && e.gv1 == gv1 && e.smem == smem) return e.clusters;
   }
   int n;
-  if (es == 2) n = gv1 ? resident_variant<2, true>(S, smem, sm_count) : resident_variant<2, false>(S, smem, sm_count);
+  if (gv1 == 2) n = es == 2 ? resident_warp_rows<2>(smem, sm_count) : resident_warp_rows<4>(smem, sm_count);
+  else if (es == 2) n = gv1 ? resident_variant<2, true>(S, smem, sm_count) : resident_variant<2, false>(S, smem, sm_count);
   else n = gv1 ? resident_variant<4, true>(S, smem, sm_count) : resident_variant<4, false>(S, smem, sm_count);
   if (g_residency_used < kResidencySlots) g_residency[g_residency_used++] = {dev, es, S, gv1, smem, n};
   return n;
@@ -339,7 +418,23 @@ cudaError_t launch_variant(const Plan& pl, cudaStream_t stream) {
 }
 
 template <int ES>
+cudaError_t launch_warp_rows(const Plan& pl, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.pub.grid_ctas), 1, 1);
+  cfg.blockDim = dim3(ds_topk_dev::kWrThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(pl.pub.smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ds_topk_dev::topk_warp_rows_kernel<ES>, pl.wprm);
+}
+
+template <int ES>
 cudaError_t launch_dtype(const Plan& pl, cudaStream_t stream) {
+  if (pl.warp_rows) return launch_warp_rows<ES>(pl, stream);
   return pl.prm.gv == 1 ? launch_variant<ES, true>(pl, stream) : launch_variant<ES, false>(pl, stream);
 }
 
@@ -371,6 +466,21 @@ extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int
   // persistent cluster walks several rows); otherwise without it.
   rc = make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, false, &pl);
   if (rc != DS_TOPK_OK) return rc;
+  if (pl.warp_rows) {
+    pl.wprm.x = static_cast<const char*>(x);
+    pl.wprm.return_value = return_value;
+    pl.wprm.out_values = return_value ? out_values : nullptr;
+    pl.wprm.out_indices = out_indices;
+    pl.wprm.flag = nan_flag;
+    const int resident_ctas = resident_cached(dev_id, pl, dev.sm_count);
+    if (resident_ctas > 0 && pl.pub.grid_ctas > resident_ctas) pl.pub.grid_ctas = resident_ctas;
+    const cudaError_t e = es == 2 ? launch_dtype<2>(pl, stream) : launch_dtype<4>(pl, stream);
+    if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) {
+      cudaGetLastError();
+      return DS_TOPK_ECUDA;
+    }
+    return DS_TOPK_OK;
+  }
   int resident = resident_cached(dev_id, pl, dev.sm_count);
   if (resident > 0 && batch > resident) {
     Plan ps;

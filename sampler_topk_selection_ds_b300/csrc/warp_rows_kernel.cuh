@@ -1,0 +1,750 @@
+// warp_rows_kernel.cuh — multi-row path: one warp selects one row, a CTA holds
+// kWrWarps rows at a time, and a persistent grid walks the batch.
+//
+// For many short rows (the decode-shaped indexer call: thousands of rows of a
+// few ten thousand elements) a whole CTA per row spends most of its time in
+// CTA-wide barriers between short phases. Here every row is owned by a single
+// warp, so all coordination is warp-synchronous (ballots, shuffles,
+// __syncwarp) and the SM keeps dozens of independent rows in flight, which is
+// what hides HBM latency. Per row:
+//
+//  T  threshold t (an order key): the warp's previous row's k-th key lowered by
+//     a margin, or, for a warp's first row, a value read off a strided sample
+//     of vector maxima. t is only a guess; the step below checks it.
+//  S  stream the row once with coalesced 16-byte loads (vector v of the row is
+//     loaded by lane v mod 32); a vector whose NaN-propagating maximum reaches
+//     t is listed (ballot + popc, so the list stays in index order) and its
+//     data parked in a small shared-memory ring. Every 32 listed vectors the
+//     warp extracts their elements >= t (or NaN) as candidates, again in index
+//     order. The guess holds iff k <= candidates <= capacity: then the
+//     candidates contain the row's top k.
+//  R  exact k-th key K* among the candidates: 256-bin histogram levels over
+//     the key range [t, max], each level narrowing the range by 8 bits.
+//  C  one ordered pass over the candidates: keep key > K*, and keys == K*
+//     while their running count stays below the ties still needed; outputs
+//     are written in ascending index order (sorted_index costs nothing).
+//
+// A row whose guess fails is retried with the sample threshold; a row that
+// still fails (massive ties, a NaN, k close to the row length) takes the exact
+// fallback: 8-bit radix levels over every element of the row, then one ordered
+// output pass. Rows with a NaN set the device flag there.
+//
+// Sources: deepseek.csdn.net, "DeepSeek 一次开源三个仓库", section 三 (算子层):
+// the threshold filter into a candidate buffer and its compaction to K;
+// deepseek-v4-pro.uk (zh-tw), "深入 DeepSeek V4.1 全新開放推論工具包", section
+// "DeepSelect：快速且刻意狹義的 TopK": bf16 and fp32, k <= 4096, the always-on
+// NaN check; github-research.aiutil.com, "deepseek-ai/DeepSelect", section
+// 关键技术亮点: batch sizes from 1 upwards and effective memory bandwidth as the
+// metric (every row is read from HBM once on the common path).
+#pragma once
+
+#include "topk_kernel.cuh"
+
+namespace ds_topk_dev {
+
+constexpr int kWrWarps = 8;                // rows in flight per CTA
+constexpr int kWrThreads = 32 * kWrWarps;
+constexpr int kWrU = 4;                    // 16-byte loads in flight per lane (direct passes)
+constexpr int kWrMaxLen = 65536;           // candidate indices are kept in 16 bits
+constexpr int kWrMaxK = 1024;
+constexpr int kWrRing = 64;                // listed vectors parked per warp
+constexpr int kWrSampleBlocks = 16;        // first-row sample: 16 blocks of 32 vectors
+constexpr int kWrChunk = 2048;             // bytes per bulk copy of a row (128 vectors)
+constexpr int kWrChunkVecs = kWrChunk / 16;
+constexpr int kWrMaxDepth = 3;             // chunks in flight per warp
+constexpr uint32_t kWrWaitLimit = 1u << 22;  // bounded mbarrier polls
+constexpr uint32_t kWrSuspendNs = 1000;      // a poll may sleep this long before it fails
+
+struct WrParams {
+  const char* x;
+  int64_t batch;
+  int64_t row_stride_bytes;
+  int32_t len;
+  int32_t nvec;           // ceil(len / VEC)
+  int32_t cap;            // candidate slots per warp (multiple of 32)
+  int32_t depth;          // chunks of the streaming ring (2 or 3)
+  int32_t k;
+  int32_t return_value;
+  void* out_values;
+  int32_t* out_indices;
+  int32_t* flag;
+};
+
+// Per-warp shared memory: streaming ring (depth x 2 KB) | ring of listed vectors
+// (also the 256-bin histogram: the two are never live at once) | their vector
+// indices | mbarriers | candidate words | candidate indices (fp32 only). bf16
+// candidate word: input bits | index << 16; fp32: input bits, index apart.
+constexpr int kWrFixedBytes = kWrRing * 16 + kWrRing * 2 + 32;
+__host__ __device__ constexpr int64_t wr_warp_bytes(int es, int64_t cap, int depth) {
+  return depth * kWrChunk + kWrFixedBytes + cap * 4 + (es == 4 ? cap * 2 : 0);
+}
+
+template <int ES>
+__device__ __forceinline__ uint32_t wr_key_floor() {
+  return ES == 2 ? 0x0080u : 0x00800000u;  // key(-inf)
+}
+
+// NaN-propagating maximum of a vector, packed (bf16x2 or one f32).
+template <int ES>
+__device__ __forceinline__ uint32_t vec_max(const uint4& w) {
+  if constexpr (ES == 2) {
+    return bf16x2_max_nan(bf16x2_max_nan(w.x, w.y), bf16x2_max_nan(w.z, w.w));
+  } else {
+    return f32_max_nan(f32_max_nan(w.x, w.y), f32_max_nan(w.z, w.w));
+  }
+}
+
+// Does some element of the vector reach the threshold (or is NaN)?
+template <int ES>
+__device__ __forceinline__ bool vec_reaches(uint32_t vmax, float tval, uint32_t tv2) {
+  if constexpr (ES == 2) {
+    uint32_t r;
+    asm("{\n\t.reg .pred lo, hi;\n\t"
+        "setp.geu.bf16x2 lo|hi, %1, %2;\n\t"
+        "or.pred lo, lo, hi;\n\t"
+        "selp.u32 %0, 1, 0, lo;\n\t}"
+        : "=r"(r) : "r"(vmax), "r"(tv2));
+    return r != 0;
+  } else {
+    (void)tv2;
+    return !(__uint_as_float(vmax) < tval);
+  }
+}
+
+// ---- bulk copies into shared memory, completed through an mbarrier ----------------
+__device__ __forceinline__ uint32_t smem_addr(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* m, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(m)), "r"(count) : "memory");
+}
+// One arrival that also announces `bytes` of incoming copies, then the copy of
+// `bytes` (a multiple of 16, both addresses 16-byte aligned) that completes them.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* m) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(m)), "r"(bytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(m))
+      : "memory");
+}
+// Polls the mbarrier phase with the given parity at most kWrWaitLimit times.
+__device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity) {
+  const uint32_t a = smem_addr(m);
+  for (uint32_t i = 0; i < kWrWaitLimit; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(a), "r"(parity), "r"(kWrSuspendNs) : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+// Bins [8*lane, 8*lane+8) of a 256-bin histogram; returns the bin b with
+//   sum(h[> b]) < need <= sum(h[>= b])
+// (the bin of the need-th largest key) and sum(h[> b]) in *above. The caller
+// guarantees sum(h) >= need. Warp-synchronous.
+__device__ __forceinline__ uint32_t wr_find_bin(const uint32_t* h, uint32_t need, uint32_t* above,
+                                                uint32_t* count) {
+  const int lane = threadIdx.x & 31;
+  const uint4 c0 = reinterpret_cast<const uint4*>(h)[lane * 2];
+  const uint4 c1 = reinterpret_cast<const uint4*>(h)[lane * 2 + 1];
+  const uint32_t c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  uint32_t s = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) s += c[j];
+  uint32_t suf = s;  // sum over lanes >= lane
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+    if (lane + o < 32) suf += t;
+  }
+  const uint32_t above_lane = suf - s;
+  const bool mine = above_lane < need && need <= suf;
+  uint32_t bin = 0, ab = 0, cnt = 0;
+  if (mine) {
+    uint32_t run = above_lane;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+      if (run + c[j] >= need) {
+        bin = static_cast<uint32_t>(lane * 8 + j);
+        ab = run;
+        cnt = c[j];
+        break;
+      }
+      run += c[j];
+    }
+  }
+  const uint32_t who = __ballot_sync(0xFFFFFFFFu, mine);
+  const int src = who ? __ffs(who) - 1 : 0;
+  *above = __shfl_sync(0xFFFFFFFFu, ab, src);
+  *count = __shfl_sync(0xFFFFFFFFu, cnt, src);
+  return __shfl_sync(0xFFFFFFFFu, bin, src);
+}
+
+__device__ __forceinline__ void wr_clear_hist(uint32_t* h) {
+  const int lane = threadIdx.x & 31;
+  reinterpret_cast<uint4*>(h)[lane * 2] = make_uint4(0, 0, 0, 0);
+  reinterpret_cast<uint4*>(h)[lane * 2 + 1] = make_uint4(0, 0, 0, 0);
+  __syncwarp();
+}
+
+template <int ES>
+struct WarpRow {
+  using T = Traits<ES>;
+  static constexpr int VEC = T::kVec;
+  static constexpr int KB = T::kKeyBits;
+  static constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+  const WrParams& p;
+  uint4* chunks;  // streaming ring, depth x kWrChunkVecs vectors
+  uint4* ring;    // listed vectors
+  uint16_t* ring_v;
+  uint32_t* hist;
+  uint64_t* mbar;
+  uint32_t* cw;   // candidate words
+  uint16_t* ci;   // candidate indices (fp32)
+  int lane;
+  uint32_t lt;
+  int nfull;      // vectors wholly inside a row
+  int nch;        // bulk chunks per row (they cover the nfull whole vectors)
+
+  __device__ WarpRow(const WrParams& prm, unsigned char* base)
+      : p(prm),
+        chunks(reinterpret_cast<uint4*>(base)),
+        ring(reinterpret_cast<uint4*>(base + prm.depth * kWrChunk)),
+        ring_v(reinterpret_cast<uint16_t*>(base + prm.depth * kWrChunk + kWrRing * 16)),
+        hist(reinterpret_cast<uint32_t*>(base + prm.depth * kWrChunk)),
+        mbar(reinterpret_cast<uint64_t*>(base + prm.depth * kWrChunk + kWrRing * 18)),
+        cw(reinterpret_cast<uint32_t*>(base + prm.depth * kWrChunk + kWrFixedBytes)),
+        ci(reinterpret_cast<uint16_t*>(base + prm.depth * kWrChunk + kWrFixedBytes) + 2 * prm.cap),
+        lane(threadIdx.x & 31),
+        lt(lanemask_lt()),
+        nfull(prm.len / VEC),
+        nch((prm.len / VEC + kWrChunkVecs - 1) / kWrChunkVecs) {}
+
+  __device__ __forceinline__ uint4 load(const char* rowp, int v) const {
+    if ((v + 1) * VEC <= p.len) return ld_nc_v4(rowp + static_cast<int64_t>(v) * 16);
+    return load_vec<ES>(rowp, v, p.len);
+  }
+
+  // Top 16 bits of the key of a packed maximum (bf16: the key itself).
+  __device__ __forceinline__ uint32_t key16(uint32_t vmax) const {
+    const uint32_t k = key_of<ES>(finish_max<ES>(vmax));
+    return ES == 2 ? k : (k >> 16);
+  }
+
+  // ---- T: first-row threshold from a sample of vector maxima ----------------------
+  // Rows of at most 512 vectors are read whole, and the threshold is exact: the
+  // k-th largest vector maximum, which at least k elements reach. Longer rows
+  // are sampled in 16 evenly spaced blocks of 32 consecutive vectors (coalesced,
+  // 1/8 of a 64 KB row's cache lines, which the stream then finds in L2), and the
+  // threshold is the q-th largest sampled maximum, q about 1.2 k times the
+  // sampled fraction plus a margin: a guess that the stream verifies.
+  __device__ __forceinline__ int sample_size() const {
+    return p.nvec <= 32 * kWrSampleBlocks ? p.nvec : 32 * kWrSampleBlocks;
+  }
+  // The rank q of the sampled maximum used as the first-row threshold.
+  __device__ __forceinline__ uint32_t default_rank() const {
+    if (p.nvec <= 32 * kWrSampleBlocks) return static_cast<uint32_t>(p.k);
+    return static_cast<uint32_t>((static_cast<int64_t>(6 * p.k) * sample_size() / 5 + p.nvec - 1) / p.nvec + 8);
+  }
+  // A rank for a second try after the threshold of rank q gave n candidates:
+  // candidates grow about in proportion to q.
+  __device__ __forceinline__ uint32_t adapted_rank(uint32_t q, int n) const {
+    uint32_t r;
+    if (n > p.cap) r = static_cast<uint32_t>(static_cast<int64_t>(q) * (3 * p.cap / 4) / n);
+    else r = static_cast<uint32_t>(static_cast<int64_t>(q) * (5 * p.k / 4) / (n > 0 ? n : 1)) + 4;
+    return r < 1u ? 1u : r;
+  }
+  __device__ uint32_t sample_threshold(const char* rowp, uint32_t q) const {
+    const int nvec = p.nvec;
+    constexpr int kPer = kWrSampleBlocks;  // vectors per lane
+    const bool whole = nvec <= 32 * kPer;
+    const int ns = whole ? nvec : 32 * kPer;
+    const int bstride = whole ? 32 : (nvec - 32) / (kPer - 1);  // block starts: i * bstride
+    if (q > static_cast<uint32_t>(ns)) return wr_key_floor<ES>();
+    uint32_t kk[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int v = i * bstride + lane;
+      kk[i] = (whole ? v < nvec : true) ? key16(vec_max<ES>(load(rowp, v))) : 0xFFFFFFFFu;
+    }
+    wr_clear_hist(hist);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (kk[i] != 0xFFFFFFFFu) atomicAdd(&hist[kk[i] >> 8], 1u);
+    __syncwarp();
+    uint32_t above, cnt;
+    const uint32_t b1 = wr_find_bin(hist, q, &above, &cnt);
+    __syncwarp();
+    wr_clear_hist(hist);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (kk[i] != 0xFFFFFFFFu && (kk[i] >> 8) == b1) atomicAdd(&hist[kk[i] & 0xFFu], 1u);
+    __syncwarp();
+    const uint32_t b2 = wr_find_bin(hist, q - above, &above, &cnt);
+    __syncwarp();
+    uint32_t t = (b1 << 8) | b2;
+    if constexpr (ES == 4) t <<= 16;
+    return t < wr_key_floor<ES>() ? wr_key_floor<ES>() : t;
+  }
+
+  __device__ __forceinline__ void put(int pos, uint32_t bits, int idx) const {
+    if constexpr (ES == 2) {
+      cw[pos] = bits | (static_cast<uint32_t>(idx) << 16);
+    } else {
+      cw[pos] = bits;
+      ci[pos] = static_cast<uint16_t>(idx);
+    }
+  }
+  __device__ __forceinline__ uint32_t bits_at(int pos) const {
+    return ES == 2 ? (cw[pos] & 0xFFFFu) : cw[pos];
+  }
+  __device__ __forceinline__ int idx_at(int pos) const {
+    return ES == 2 ? static_cast<int>(cw[pos] >> 16) : static_cast<int>(ci[pos]);
+  }
+
+  // ---- S: listing and candidate extraction under a threshold key ------------------
+  struct Lister {
+    float tval;
+    uint32_t tv2;
+    int wpos, rpos, ccount;  // warp-uniform
+    bool nan;                // per lane
+    uint32_t kmax;           // per lane: largest key of the lane's listed vectors
+  };
+  __device__ __forceinline__ Lister lister(uint32_t tk) const {
+    Lister L;
+    L.tval = key_threshold_value<ES>(tk);
+    L.tv2 = (__float_as_uint(L.tval) >> 16) * 0x00010001u;
+    L.wpos = L.rpos = L.ccount = 0;
+    L.nan = false;
+    L.kmax = 0;
+    return L;
+  }
+
+  // Elements >= t (or NaN) of `cnt` listed vectors starting at ring slot L.rpos
+  // (one vector per lane), appended in index order at candidate position
+  // L.ccount (writes stop at cap). Every element slot is written by a static,
+  // predicated store, so lanes never diverge.
+  __device__ __forceinline__ void extract(Lister& L, int cnt) const {
+    const bool has = lane < cnt;
+    const int slot = (L.rpos + lane) & (kWrRing - 1);
+    uint4 w = make_uint4(0, 0, 0, 0);
+    int v = 0;
+    uint32_t m = 0;
+    if (has) {
+      w = ring[slot];
+      v = ring_v[slot];
+      m = cand_mask<ES>(w, L.tval, L.tv2);
+      const int rem = p.len - v * VEC;
+      if (rem < VEC) m &= (1u << rem) - 1u;
+      // a NaN element makes the maximum NaN; otherwise the maximum's key
+      // bounds the keys of the row's candidates from above
+      const uint32_t mx = finish_max<ES>(vec_max<ES>(w));
+      L.nan |= is_nan_bits<ES>(mx);
+      L.kmax = max(L.kmax, key_of<ES>(mx));
+    }
+    const uint32_t c = __popc(m);
+    const uint32_t pre = warp_excl_scan(c);
+    const int tot = static_cast<int>(__shfl_sync(kFull, pre + c, 31));
+    int pos = L.ccount + static_cast<int>(pre);
+    const int ib = v * VEC;
+    if (L.ccount + 32 * VEC <= p.cap) {  // warp-uniform: room for a whole round
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        if (m & (1u << e)) put(pos++, elem_bits<ES>(w, e), ib + e);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        if (m & (1u << e)) {
+          if (pos < p.cap) put(pos, elem_bits<ES>(w, e), ib + e);
+          ++pos;
+        }
+      }
+    }
+    L.ccount += tot;
+    L.rpos += cnt;
+  }
+
+  // One vector per lane (vector v of the row, valid if `in`): list it if it
+  // reaches the threshold; every 32 listed vectors, extract their candidates.
+  __device__ __forceinline__ void step(Lister& L, const uint4& w, int v, bool in) const {
+    const bool pass = in && vec_reaches<ES>(vec_max<ES>(w), L.tval, L.tv2);
+    const uint32_t b = __ballot_sync(kFull, pass);
+    if (pass) {
+      const int slot = (L.wpos + __popc(b & lt)) & (kWrRing - 1);
+      ring[slot] = w;
+      ring_v[slot] = static_cast<uint16_t>(v);
+    }
+    L.wpos += __popc(b);
+    if (L.wpos - L.rpos >= 32) {
+      __syncwarp();
+      extract(L, 32);
+      __syncwarp();
+    }
+  }
+  // Returns the number of candidates (it may exceed cap; writes stop there).
+  __device__ __forceinline__ int finish(Lister& L) const {
+    if (L.wpos > L.rpos) {
+      __syncwarp();
+      extract(L, L.wpos - L.rpos);
+      __syncwarp();
+    }
+    return L.ccount;
+  }
+
+  // The listing pass reading the row directly from global memory (retries).
+  __device__ int direct_pass(const char* rowp, uint32_t tk, bool* nan, uint32_t* kmax) const {
+    Lister L = lister(tk);
+    const int nsteps = (p.nvec + 31) / 32;
+    for (int i0 = 0; i0 < nsteps; i0 += kWrU) {
+      uint4 w[kWrU];
+#pragma unroll
+      for (int u = 0; u < kWrU; ++u) {
+        const int v = (i0 + u) * 32 + lane;
+        w[u] = v < p.nvec ? load(rowp, v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kWrU; ++u) {
+        if (i0 + u >= nsteps) break;  // warp-uniform
+        const int v = (i0 + u) * 32 + lane;
+        step(L, w[u], v, v < p.nvec);
+      }
+    }
+    const int n = finish(L);
+    *nan = L.nan;
+    *kmax = __reduce_max_sync(kFull, L.kmax);
+    return n;
+  }
+
+  // ---- the streaming ring: chunks of the warp's rows, in order, depth ahead -------
+  struct Stream {
+    const char* src;    // source of the next chunk to copy (null: none left)
+    int64_t prow;       // its row
+    int pchunk;         // its chunk index in that row
+    int pslot;          // ring slot it goes to
+    int cslot;          // ring slot of the next chunk to read
+    uint32_t cphase;    // mbarrier phase parity that chunk completes
+    uint32_t issued;    // chunks copied so far
+    uint32_t consumed;  // chunks read so far
+  };
+  __device__ __forceinline__ void stream_begin(Stream& st, int64_t first) const {
+    st.prow = first;
+    st.src = (first < p.batch && nch > 0) ? p.x + first * p.row_stride_bytes : nullptr;
+    st.pchunk = st.pslot = st.cslot = 0;
+    st.cphase = st.issued = st.consumed = 0u;
+  }
+  // Copies the next chunk of the warp's row sequence into the ring, if any.
+  __device__ __forceinline__ void produce_one(Stream& st, int64_t row_step) const {
+    if (st.src == nullptr) return;
+    const bool last = st.pchunk == nch - 1;
+    const uint32_t bytes = last ? static_cast<uint32_t>(nfull * 16 - (nch - 1) * kWrChunk) : kWrChunk;
+    if (lane == 0) bulk_load(chunks + st.pslot * kWrChunkVecs, st.src, bytes, mbar + st.pslot);
+    if (++st.pslot == p.depth) st.pslot = 0;
+    ++st.issued;
+    if (last) {
+      st.pchunk = 0;
+      st.prow += row_step;
+      st.src = st.prow < p.batch ? p.x + st.prow * p.row_stride_bytes : nullptr;
+    } else {
+      ++st.pchunk;
+      st.src += kWrChunk;
+    }
+  }
+  // The listing pass over one row, fed by the ring: each chunk read frees its
+  // slot for the chunk `depth` places further on. Returns false if a copy never
+  // completed within the poll limit (the warp must then stop).
+  __device__ bool stream_pass(Stream& st, int64_t row_step, const char* rowp, uint32_t tk, int* n,
+                              bool* nan, uint32_t* kmax) const {
+    Lister L = lister(tk);
+    constexpr int kSteps = kWrChunkVecs / 32;
+    for (int c = 0; c < nch; ++c) {
+      const int slot = st.cslot;
+      if (!__all_sync(kFull, mbar_wait(mbar + slot, st.cphase))) return false;
+      if (++st.cslot == p.depth) {
+        st.cslot = 0;
+        st.cphase ^= 1u;
+      }
+      const uint4* buf = chunks + slot * kWrChunkVecs + lane;
+      const int vb = c * kWrChunkVecs + lane;
+      uint4 w[kSteps];
+      if (c < nch - 1 || nfull % kWrChunkVecs == 0) {  // a whole chunk
+#pragma unroll
+        for (int u = 0; u < kSteps; ++u) w[u] = buf[u * 32];
+        __syncwarp();  // every lane has read the slot: refill it
+        ++st.consumed;
+        produce_one(st, row_step);
+#pragma unroll
+        for (int u = 0; u < kSteps; ++u) step(L, w[u], vb + u * 32, true);
+      } else {
+#pragma unroll
+        for (int u = 0; u < kSteps; ++u) w[u] = vb + u * 32 < nfull ? buf[u * 32] : make_uint4(0, 0, 0, 0);
+        __syncwarp();
+        ++st.consumed;
+        produce_one(st, row_step);
+#pragma unroll
+        for (int u = 0; u < kSteps; ++u)
+          if (vb - lane + u * 32 < nfull) step(L, w[u], vb + u * 32, vb + u * 32 < nfull);  // warp-uniform
+      }
+    }
+    if (nfull < p.nvec) {  // the ragged last vector
+      const bool in = lane == 0;
+      const uint4 w = in ? load_vec<ES>(rowp, nfull, p.len) : make_uint4(0, 0, 0, 0);
+      step(L, w, nfull, in);
+    }
+    *n = finish(L);
+    *nan = L.nan;
+    *kmax = __reduce_max_sync(kFull, L.kmax);
+    return true;
+  }
+  // Waits (bounded) for every copy still in flight.
+  __device__ void drain(Stream& st) const {
+    while (st.consumed != st.issued) {
+      mbar_wait(mbar + st.cslot, st.cphase);
+      if (++st.cslot == p.depth) {
+        st.cslot = 0;
+        st.cphase ^= 1u;
+      }
+      ++st.consumed;
+    }
+  }
+
+  // ---- R + C on the candidates ---------------------------------------------------
+  // n candidates (k <= n <= cap), all with key >= tk, in index order.
+  // Returns the row's k-th key.
+  // kmax: the largest candidate key.
+  __device__ uint32_t select_candidates(int64_t row, int n, uint32_t tk, uint32_t kmax) const {
+    uint32_t lo = tk, hi = kmax, need = static_cast<uint32_t>(p.k);
+    for (;;) {
+      const uint32_t span = hi - lo;
+      const int s = span < 256u ? 0 : (32 - __clz(span)) - 8;
+      wr_clear_hist(hist);
+      for (int j = lane; j < n; j += 32) {
+        const uint32_t key = key_of<ES>(bits_at(j));
+        if (key >= lo && key <= hi) atomicAdd(&hist[(key - lo) >> s], 1u);
+      }
+      __syncwarp();
+      uint32_t above, cnt;
+      const uint32_t b = wr_find_bin(hist, need, &above, &cnt);
+      __syncwarp();
+      need -= above;
+      lo += b << s;
+      if (s == 0) break;
+      const uint32_t top = lo + ((1u << s) - 1u);
+      hi = top < hi ? top : hi;
+    }
+    const uint32_t kth = lo;
+    // ordered output: ties (key == kth) are taken in index order, `need` of them
+    int taken_eq = 0, out = 0;
+    const int64_t obase = row * p.k;
+    for (int j0 = 0; j0 < n && out < p.k; j0 += 32) {
+      const int j = j0 + lane;
+      uint32_t bits = 0, key = 0;
+      if (j < n) {
+        bits = bits_at(j);
+        key = key_of<ES>(bits);
+      }
+      const bool eq = j < n && key == kth;
+      const uint32_t eqb = __ballot_sync(kFull, eq);
+      const bool sel = (j < n && key > kth) ||
+                       (eq && static_cast<uint32_t>(taken_eq + __popc(eqb & lt)) < need);
+      taken_eq += __popc(eqb);
+      const uint32_t sb = __ballot_sync(kFull, sel);
+      if (sel && out + __popc(sb & lt) < p.k) {
+        const int64_t o = obase + out + __popc(sb & lt);
+        p.out_indices[o] = idx_at(j);
+        if (p.return_value) {
+          if constexpr (ES == 2) static_cast<uint16_t*>(p.out_values)[o] = static_cast<uint16_t>(bits);
+          else static_cast<uint32_t*>(p.out_values)[o] = bits;
+        }
+      }
+      out += __popc(sb);
+    }
+    return kth;
+  }
+
+  // ---- exact k-th largest vector maximum (top 16 key bits) --------------------------
+  // Two passes over the row, one histogram update per vector. At least k
+  // elements reach the result, so it is a threshold that always holds.
+  __device__ uint32_t vecmax_threshold(const char* rowp) const {
+    if (p.nvec < p.k) return wr_key_floor<ES>();
+    const int nsteps = (p.nvec + 31) / 32;
+    uint32_t need = static_cast<uint32_t>(p.k), b1 = 0;
+    for (int level = 0; level < 2; ++level) {
+      wr_clear_hist(hist);
+      for (int i = 0; i < nsteps; ++i) {
+        const int v = i * 32 + lane;
+        if (v < p.nvec) {
+          const uint32_t kk = key16(vec_max<ES>(load(rowp, v)));
+          if (level == 0) atomicAdd(&hist[kk >> 8], 1u);
+          else if ((kk >> 8) == b1) atomicAdd(&hist[kk & 0xFFu], 1u);
+        }
+      }
+      __syncwarp();
+      uint32_t above, cnt;
+      const uint32_t b = wr_find_bin(hist, need, &above, &cnt);
+      __syncwarp();
+      need -= above;
+      if (level == 0) b1 = b;
+      else b1 = (b1 << 8) | b;
+    }
+    uint32_t t = b1;
+    if constexpr (ES == 4) t <<= 16;
+    return t < wr_key_floor<ES>() ? wr_key_floor<ES>() : t;
+  }
+
+  // ---- exact fallback: radix levels over every element, then an ordered pass ------
+  __device__ void exact_row(const char* rowp, int64_t row) const {
+    const int nvec = p.nvec;
+    const int nsteps = (nvec + 31) / 32;
+    uint32_t prefix = 0, need = static_cast<uint32_t>(p.k);
+    bool nan = false;
+    for (int done = 0; done < KB; done += 8) {
+      wr_clear_hist(hist);
+      const int sh = KB - done - 8;
+      for (int i = 0; i < nsteps; ++i) {
+        const int v = i * 32 + lane;
+        if (v >= nvec) continue;
+        const uint4 w = load(rowp, v);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          if (v * VEC + e < p.len) {
+            const uint32_t bits = elem_bits<ES>(w, e);
+            if (done == 0) nan |= is_nan_bits<ES>(bits);
+            const uint32_t key = key_of<ES>(bits);
+            if (done == 0 || (key >> (sh + 8)) == prefix) atomicAdd(&hist[(key >> sh) & 0xFFu], 1u);
+          }
+        }
+      }
+      __syncwarp();
+      uint32_t above, cnt;
+      const uint32_t b = wr_find_bin(hist, need, &above, &cnt);
+      __syncwarp();
+      need -= above;
+      prefix = (prefix << 8) | b;
+    }
+    if (__any_sync(kFull, nan) && lane == 0) atomicOr(p.flag, DS_TOPK_FLAG_NAN);
+    const uint32_t kth = prefix;
+    int taken_eq = 0, out = 0;
+    const int64_t obase = row * p.k;
+    for (int i = 0; i < nsteps && out < p.k; ++i) {
+      const int v = i * 32 + lane;
+      uint4 w = make_uint4(0, 0, 0, 0);
+      uint32_t mgt = 0, meq = 0;
+      if (v < nvec) {
+        w = load(rowp, v);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          if (v * VEC + e < p.len) {
+            const uint32_t key = key_of<ES>(elem_bits<ES>(w, e));
+            mgt |= static_cast<uint32_t>(key > kth) << e;
+            meq |= static_cast<uint32_t>(key == kth) << e;
+          }
+        }
+      }
+      // ties before this lane's vector, in index order
+      const uint32_t ce = __popc(meq);
+      const uint32_t pe = warp_excl_scan(ce);
+      const uint32_t te = __shfl_sync(kFull, pe + ce, 31);
+      const int before = taken_eq + static_cast<int>(pe);
+      int take = static_cast<int>(need) - before;
+      take = take < 0 ? 0 : (take > static_cast<int>(ce) ? static_cast<int>(ce) : take);
+      uint32_t msel = mgt;
+      uint32_t mq = meq;
+      for (int t = 0; t < take; ++t) {
+        msel |= mq & (0u - mq);  // lowest remaining tie
+        mq &= mq - 1;
+      }
+      taken_eq += static_cast<int>(te);
+      const uint32_t cs = __popc(msel);
+      const uint32_t ps = warp_excl_scan(cs);
+      const int ts = static_cast<int>(__shfl_sync(kFull, ps + cs, 31));
+      int64_t o = obase + out + ps;
+      while (msel && o < obase + p.k) {
+        const int e = __ffs(msel) - 1;
+        msel &= msel - 1;
+        p.out_indices[o] = v * VEC + e;
+        if (p.return_value) {
+          const uint32_t bits = elem_bits<ES>(w, e);
+          if constexpr (ES == 2) static_cast<uint16_t*>(p.out_values)[o] = static_cast<uint16_t>(bits);
+          else static_cast<uint32_t*>(p.out_values)[o] = bits;
+        }
+        ++o;
+      }
+      out += ts;
+    }
+  }
+};
+
+// Margin (in top-16 key units) below the previous row's k-th key for the next
+// row's threshold guess.
+constexpr uint32_t kWrGuessMargin = 6;
+
+template <int ES>
+__global__ void __launch_bounds__(kWrThreads, 3) topk_warp_rows_kernel(const WrParams p) {
+  // let the next kernel in the stream start its prologue; wait for the previous one
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int warp = threadIdx.x >> 5;
+  const WarpRow<ES> wr(p, smem + warp * wr_warp_bytes(ES, p.cap, p.depth));
+  constexpr int KB = Traits<ES>::kKeyBits;
+  constexpr uint32_t kFull = 0xFFFFFFFFu;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWrWarps;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kWrWarps + warp;
+  if (wr.lane == 0) {
+    for (int i = 0; i < p.depth; ++i) mbar_init(wr.mbar + i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncwarp();
+  // the warp's rows stream through its ring back to back: the next row's first
+  // chunks are in flight while the current row is being selected
+  typename WarpRow<ES>::Stream st;
+  wr.stream_begin(st, first);
+  for (int i = 0; i < p.depth; ++i) wr.produce_one(st, nwarps);
+  bool have_guess = false;
+  uint32_t guess = 0;
+  for (int64_t row = first; row < p.batch; row += nwarps) {
+    const char* rowp = p.x + row * p.row_stride_bytes;
+    uint32_t q = wr.default_rank();
+    uint32_t tk = have_guess ? guess : wr.sample_threshold(rowp, q);
+    bool nan = false;
+    int n = 0;
+    uint32_t kmax = 0;
+    if (!wr.stream_pass(st, nwarps, rowp, tk, &n, &nan, &kmax)) {
+      if (wr.lane == 0) atomicOr(p.flag, DS_TOPK_FLAG_TIMEOUT);
+      wr.drain(st);
+      return;
+    }
+    bool bad = __any_sync(kFull, nan);
+    bool ok = !bad && n >= p.k && n <= p.cap;
+    // retries, each a direct pass over the row (from L2): the default sample
+    // rank after a carried guess, then a rank adapted to the count just seen,
+    // then the exact k-th largest vector maximum
+    for (int attempt = have_guess ? 0 : 1; !ok && !bad && attempt < 3; ++attempt) {
+      if (attempt == 1) q = wr.adapted_rank(q, n);
+      tk = attempt == 2 ? wr.vecmax_threshold(rowp) : wr.sample_threshold(rowp, q);
+      n = wr.direct_pass(rowp, tk, &nan, &kmax);
+      bad = __any_sync(kFull, nan);
+      ok = !bad && n >= p.k && n <= p.cap;
+    }
+    if (ok) {
+      const uint32_t kth = wr.select_candidates(row, n, tk, kmax);
+      const uint32_t m = (KB == 16 ? kWrGuessMargin : (kWrGuessMargin << 16));
+      guess = kth > wr_key_floor<ES>() + m ? kth - m : wr_key_floor<ES>();
+      have_guess = true;
+    } else {
+      wr.exact_row(rowp, row);
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace ds_topk_dev

@@ -75,9 +75,21 @@ def test_batch_zero_is_ok_without_pointers():
 
 
 def test_plan_shapes():
+    # many short rows: one warp per row, 8 rows per CTA, ~2k candidate slots per warp
     rc, p = dstk.ds_topk_plan(dstk.BF16, 16384, 32768, 32768, 512, 148)
-    assert rc == 0 and p.path == dstk.PATH_ROW and p.cluster_size == 1
-    assert p.grid_ctas == 16384 and p.vectors_per_granule == 1 and p.launches == 1
+    assert rc == 0 and p.path == dstk.PATH_WARP_ROWS and p.cluster_size == 1
+    assert p.grid_ctas == 16384 // 8 and p.threads_per_cta == 256 and p.launches == 1
+    assert p.granules_per_cta == 1024 and 3 * (p.smem_bytes + 1024) <= 228 * 1024  # 3 CTAs per SM
+    # fewer than 8 rows per SM: one CTA per row
+    rc, p = dstk.ds_topk_plan(dstk.BF16, 1000, 32768, 32768, 512, 148)
+    assert rc == 0 and p.path == dstk.PATH_ROW and p.grid_ctas == 1000
+    assert p.vectors_per_granule == 1
+    # warp path limits: 16-bit candidate indices, and its shared memory
+    assert dstk.ds_topk_plan(dstk.BF16, 4096, 65537, 65544, 512, 148)[1].path == dstk.PATH_ROW
+    assert dstk.ds_topk_plan(dstk.BF16, 4096, 65536, 65536, 2048, 148)[1].path == dstk.PATH_ROW
+    assert dstk.ds_topk_plan(dstk.FP32, 4096, 65536, 65536, 1024, 148)[1].path == dstk.PATH_ROW
+    rc, p = dstk.ds_topk_plan(dstk.FP32, 4096, 100, 100, 100, 148)
+    assert rc == 0 and p.path == dstk.PATH_WARP_ROWS and p.granules_per_cta == 128
     rc, p = dstk.ds_topk_plan(dstk.FP32, 64, 129280, 129280, 512, 148)
     assert rc == 0 and p.path == dstk.PATH_CLUSTER and p.cluster_size in (2, 4, 8, 16)
     assert p.grid_ctas == 64 * p.cluster_size
