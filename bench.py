@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import glob
 import hashlib
 import io
 import json
@@ -41,8 +42,15 @@ METRIC = "effective HBM GB/s and rows/s for batched TopK (bf16 indexer, fp32 sam
 DEFAULT_WORKLOAD = "c2"
 L2_BYTES_FALLBACK = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6400.0
-KERNEL_SOURCES = ["sampler_topk_selection_ds_b300/csrc/topk_kernel.cuh",
-                  "sampler_topk_selection_ds_b300/csrc/ds_topk.cu"]
+KERNEL_SOURCES = sorted(os.path.relpath(f, ROOT) for f in
+                        glob.glob(os.path.join(ROOT, "sampler_topk_selection_ds_b300", "csrc", "*.cu*")))
+
+
+def kernel_name(w, plan) -> str:
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    if plan.path == 2:
+        return f"topk_warp_rows_kernel<{es}>"
+    return f"topk_rows_kernel<{es},{plan.cluster_size}>"
 
 
 def kernel_hash() -> str:
@@ -334,7 +342,7 @@ def run_ours(args, w):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": peak_src + (" (of measured)" if peak_src != "fallback" else " (of fallback)"),
                          "traffic": traffic, "traffic_note": traffic_note,
-                         "kernel": f"topk_rows_kernel<{2 if w.dtype == torch.bfloat16 else 4},{plan.cluster_size}>",
+                         "kernel": kernel_name(w, plan),
                          "kernel_hash": kernel_hash()},
             "e2e": e2e,
             "gpu_launches": args.steps * plan.launches,

@@ -14,10 +14,10 @@
 //      threshold to the minimum of K survivors), computed from all granules at
 //      once instead of raised along a randomised scan.
 //  L   list, in index order, the granules whose maximum reaches t.
-//  B   exact k-th key K* among the elements >= t: 8-bit radix levels from the
-//      most significant digit (2 levels for bf16 keys, 4 for fp32), histograms
-//      aggregated per warp with match.any and summed over the cluster through
-//      distributed shared memory.
+//  B   exact k-th key K* among the elements >= t: shared-memory histogram
+//      levels over the candidate keys (a 256-key window starting at t, then
+//      8-bit digits), summed over the cluster through distributed shared memory
+//      where the candidates are spread over the cluster's CTAs.
 //  C   ordered compaction: every element with key > K*, plus the lowest-index
 //      elements with key == K* until k are taken, written in ascending index
 //      order (so sorted_index costs nothing).

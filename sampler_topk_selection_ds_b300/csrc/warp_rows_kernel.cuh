@@ -94,21 +94,25 @@ __device__ __forceinline__ uint32_t vec_max(const uint4& w) {
   }
 }
 
-// Does some element of the vector reach the threshold (or is NaN)?
+// Ballot over the warp of "some element of the lane's vector reaches the
+// threshold (or is NaN)", for lanes with `in` set.
 template <int ES>
-__device__ __forceinline__ bool vec_reaches(uint32_t vmax, float tval, uint32_t tv2) {
+__device__ __forceinline__ uint32_t ballot_reaches(uint32_t vmax, float tval, uint32_t tv2, bool in) {
+  uint32_t b;
   if constexpr (ES == 2) {
-    uint32_t r;
-    asm("{\n\t.reg .pred lo, hi;\n\t"
+    asm volatile(
+        "{\n\t.reg .pred lo, hi, q;\n\t"
+        "setp.ne.u32 q, %3, 0;\n\t"
         "setp.geu.bf16x2 lo|hi, %1, %2;\n\t"
         "or.pred lo, lo, hi;\n\t"
-        "selp.u32 %0, 1, 0, lo;\n\t}"
-        : "=r"(r) : "r"(vmax), "r"(tv2));
-    return r != 0;
+        "and.pred lo, lo, q;\n\t"
+        "vote.sync.ballot.b32 %0, lo, 0xffffffff;\n\t}"
+        : "=r"(b) : "r"(vmax), "r"(tv2), "r"(static_cast<uint32_t>(in)));
   } else {
     (void)tv2;
-    return !(__uint_as_float(vmax) < tval);
+    b = __ballot_sync(0xFFFFFFFFu, in && !(__uint_as_float(vmax) < tval));
   }
+  return b;
 }
 
 // ---- bulk copies into shared memory, completed through an mbarrier ----------------
@@ -355,9 +359,22 @@ struct WarpRow {
     int pos = L.ccount + static_cast<int>(pre);
     const int ib = v * VEC;
     if (L.ccount + 32 * VEC <= p.cap) {  // warp-uniform: room for a whole round
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      uint32_t* dst = cw + pos;
+      if constexpr (ES == 2) {
+        // candidate word = element bits | index << 16: one byte permute each
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        if (m & (1u << e)) put(pos++, elem_bits<ES>(w, e), ib + e);
+        for (int e = 0; e < VEC; ++e)
+          if (m & (1u << e)) *dst++ = __byte_perm(ws[e >> 1], static_cast<uint32_t>(ib + e), (e & 1) ? 0x5432 : 0x5410);
+      } else {
+        uint16_t* di = ci + pos;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          if (m & (1u << e)) {
+            *dst++ = ws[e];
+            *di++ = static_cast<uint16_t>(ib + e);
+          }
+        }
       }
     } else {
 #pragma unroll
@@ -375,9 +392,9 @@ struct WarpRow {
   // One vector per lane (vector v of the row, valid if `in`): list it if it
   // reaches the threshold; every 32 listed vectors, extract their candidates.
   __device__ __forceinline__ void step(Lister& L, const uint4& w, int v, bool in) const {
-    const bool pass = in && vec_reaches<ES>(vec_max<ES>(w), L.tval, L.tv2);
-    const uint32_t b = __ballot_sync(kFull, pass);
-    if (pass) {
+    const uint32_t b = ballot_reaches<ES>(vec_max<ES>(w), L.tval, L.tv2, in);
+    if (b == 0u) return;  // warp-uniform: nothing listed in this step
+    if (b & (1u << lane)) {
       const int slot = (L.wpos + __popc(b & lt)) & (kWrRing - 1);
       ring[slot] = w;
       ring_v[slot] = static_cast<uint16_t>(v);
@@ -713,8 +730,8 @@ __global__ void __launch_bounds__(kWrThreads, 3) topk_warp_rows_kernel(const WrP
   uint32_t guess = 0;
   for (int64_t row = first; row < p.batch; row += nwarps) {
     const char* rowp = p.x + row * p.row_stride_bytes;
-    uint32_t q = wr.default_rank();
-    uint32_t tk = have_guess ? guess : wr.sample_threshold(rowp, q);
+    uint32_t q = 0;
+    uint32_t tk = have_guess ? guess : wr.sample_threshold(rowp, q = wr.default_rank());
     bool nan = false;
     int n = 0;
     uint32_t kmax = 0;
@@ -729,6 +746,7 @@ __global__ void __launch_bounds__(kWrThreads, 3) topk_warp_rows_kernel(const WrP
     // rank after a carried guess, then a rank adapted to the count just seen,
     // then the exact k-th largest vector maximum
     for (int attempt = have_guess ? 0 : 1; !ok && !bad && attempt < 3; ++attempt) {
+      if (attempt == 0) q = wr.default_rank();
       if (attempt == 1) q = wr.adapted_rank(q, n);
       tk = attempt == 2 ? wr.vecmax_threshold(rowp) : wr.sample_threshold(rowp, q);
       n = wr.direct_pass(rowp, tk, &nan, &kmax);
