@@ -37,9 +37,14 @@ constexpr int64_t kSmemPerSm = 228 * 1024;
 constexpr int64_t kSmemPerCtaReserved = 1024;
 // Most vectors per thread held in the next-row prefetch buffer.
 constexpr int64_t kMaxStageVecs = 16;
-// The one-warp-per-row path is taken from this many rows per SM on (below it a
-// whole CTA per row finishes a row sooner than a warp does).
-constexpr int64_t kWrMinRowsPerSm = 8;
+// The one-warp-per-row path is taken from this many rows per SM on: a warp needs
+// about as long for one row as a CTA needs for several, so the warps of every SM
+// must have rows to share. Measured crossover: about 32 rows per SM for rows of
+// 32K bf16 elements; shorter rows cross over sooner.
+int64_t wr_min_rows_per_sm(int64_t len) {
+  int64_t r = len / 1024;
+  return r < 4 ? 4 : (r > 32 ? 32 : r);
+}
 
 struct Plan {
   ds_topk_plan_t pub;
@@ -77,7 +82,7 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
   // Many short rows: one warp per row (candidate indices fit 16 bits, and a
   // warp's candidate buffer of about 2k entries leaves room for 2+ CTAs per SM).
   if (len <= ds_topk_dev::kWrMaxLen && k <= ds_topk_dev::kWrMaxK &&
-      batch >= kWrMinRowsPerSm * static_cast<int64_t>(sm_count)) {
+      batch >= wr_min_rows_per_sm(len) * static_cast<int64_t>(sm_count)) {
     int64_t cap = 2 * static_cast<int64_t>(k) + 256;
     if (cap > static_cast<int64_t>(k) + 512) cap = static_cast<int64_t>(k) + 512;
     cap = (cap + 31) / 32 * 32;

@@ -989,10 +989,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       const int sbase = static_cast<int>(misc[kSegBase + warp]);
       const int scnt = static_cast<int>(misc[kSegCnt + warp]);
       uint32_t need = k, kstar = 0, small = 0;
-      uint32_t wbase = t16;
+      const uint32_t wbase = t16;
       uint32_t* ovl = misc + kOvl;
-#pragma unroll 1
-      while (true) {  // windowed level on the top 16 key bits, moving up from t16
+      {  // windowed level on the top 16 key bits: the 256 values from t16 up
         if (tid < kRadix) hloc[tid] = 0;
         if (tid == 0) *ovl = 0;
         __syncthreads();
@@ -1009,13 +1008,34 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         __syncthreads();
         const LevelResult r = scan_level(hloc, *ovl, bc, need);
         if (r.shift && wbase + 256u <= 0xFFFFu) {
-          wbase += 256u;
-          continue;
+          // the k-th key lies above the window: two 8-bit levels over the top 16
+          // key bits of the candidates above it
+          const uint32_t lo16 = wbase + 256u;
+          uint32_t hi8 = 0;
+#pragma unroll 1
+          for (int lv = 0; lv < 2; ++lv) {
+            if (tid < kRadix) hloc[tid] = 0;
+            __syncthreads();
+            for (int c = lane; c < scnt; c += 32) {
+              const uint32_t k16v = cand_key<ES>(c0[sbase + c]) >> (KB - 16);
+              const bool ok = k16v >= lo16 && (lv == 0 || (k16v >> 8) == hi8);
+              hist_add(hloc, lv == 0 ? (k16v >> 8) : (k16v & 0xFFu), ok);
+            }
+            __syncthreads();
+            const LevelResult rl = scan_level(hloc, 0u, bc, need);
+            need -= rl.above;
+            if (lv == 0) {
+              hi8 = rl.digit;
+            } else {
+              kstar = ((hi8 << 8) | rl.digit) << (KB - 16);
+              small = rl.count;
+            }
+          }
+        } else {
+          kstar = (wbase + r.digit) << (KB - 16);
+          need -= r.above;
+          small = r.count;
         }
-        kstar = (wbase + r.digit) << (KB - 16);
-        need -= r.above;
-        small = r.count;
-        break;
       }
       if constexpr (KB == 32) {
         const uint32_t pre16 = kstar >> 16;
@@ -1123,9 +1143,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         }
       };
       uint32_t need = k, kstar = 0;
-      uint32_t wbase = t16;
-#pragma unroll 1
-      while (true) {
+      {
+        // the 256 top-16 key values from t16 up, with a count of the keys above
+        const uint32_t wbase = t16;
         CL.begin();
         uint32_t* h = CL.loc();
         uint32_t lover = 0;
@@ -1139,12 +1159,31 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         if (lane == 0 && lover) atomicAdd(CL.ov(), lover);
         const LevelResult r = CL.finish<S>(lvl++, need);
         if (r.shift && wbase + 256u <= 0xFFFFu) {
-          wbase += 256u;
-          continue;
+          // the k-th key lies above the window (t far below it, e.g. when k exceeds
+          // the number of granules with a finite maximum): two 8-bit levels over
+          // the top 16 key bits of the keys above the window
+          const uint32_t lo16 = wbase + 256u;
+          CL.begin();
+          h = CL.loc();
+          visit([&](uint32_t key, bool ok) {
+            const uint32_t k16v = key >> (KB - 16);
+            hist_add(h, k16v >> 8, ok && k16v >= lo16);
+          });
+          const LevelResult ra = CL.finish<S>(lvl++, need);
+          need -= ra.above;
+          CL.begin();
+          h = CL.loc();
+          visit([&](uint32_t key, bool ok) {
+            const uint32_t k16v = key >> (KB - 16);
+            hist_add(h, k16v & 0xFFu, ok && k16v >= lo16 && (k16v >> 8) == ra.digit);
+          });
+          const LevelResult rb = CL.finish<S>(lvl++, need);
+          need -= rb.above;
+          kstar = ((ra.digit << 8) | rb.digit) << (KB - 16);
+        } else {
+          kstar = (wbase + r.digit) << (KB - 16);
+          need -= r.above;
         }
-        kstar = (wbase + r.digit) << (KB - 16);
-        need -= r.above;
-        break;
       }
       if constexpr (KB == 32) {
 #pragma unroll 1

@@ -231,3 +231,17 @@ def test_invariants_on_gpu_output_c3():
     gv, gi, gf = run_gpu(x, w.k, True, True)
     for b in range(w.batch):
         check_invariants(x[b], w.k, gi[b].numpy(), bits_of(gv[b]))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_k_beyond_finite_granules(dtype):
+    """k above the number of vectors holding a finite value: the granule threshold is
+    -inf, every element is a candidate, and the selection must still resolve the
+    k-th key directly (one CTA per row, and a cluster per row)."""
+    x = workloads.random_rows(64, 4096, dtype, 4096, style="normal")
+    x[:, 3072:] = float("-inf")          # 3072 finite values, 384 (bf16) / 768 (fp32) vectors
+    for k in (512, 1024):
+        assert_parity(x, k, sorted_index=False, return_value=True)
+    x = workloads.random_rows(2, 300000, dtype, 4097, style="normal")
+    x[:, 2000:] = float("-inf")
+    assert_parity(x, 4096, sorted_index=True, return_value=True)

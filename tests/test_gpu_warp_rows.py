@@ -1,7 +1,7 @@
 """GPU parity of the one-warp-per-row path (many rows of at most 65536 elements).
 
-The path is chosen from 8 rows per SM on, so every batch here has at least that
-many rows; each test first checks through ds_topk_plan that the call really runs
+The path is chosen from 4 to 32 rows per SM on (more for longer rows), so every
+batch here has at least that many rows; each test first checks through ds_topk_plan that the call really runs
 on that path. Rows are mixed so that the threshold a warp carries from one row
 to the next is often wrong (the retry and the exact fallback then run too).
 """
@@ -26,8 +26,9 @@ def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-def _wr_batch():
-    return 8 * _sms() + 5  # a ragged last CTA
+def _wr_batch(length):
+    # the path needs min(32, max(4, len / 1024)) rows per SM; +5 leaves a ragged last CTA
+    return min(32, max(4, length // 1024)) * _sms() + 5
 
 
 def _assert_path(x, k, length=None):
@@ -58,7 +59,7 @@ WR_SHAPES = [
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("length,ks", WR_SHAPES)
 def test_warp_rows_normal(dtype, length, ks):
-    x = workloads.random_rows(_wr_batch(), length, dtype, 500 + length, style="normal")
+    x = workloads.random_rows(_wr_batch(length), length, dtype, 500 + length, style="normal")
     for k in ks:
         if dtype == torch.float32 and k > 512 and length > 2304:
             continue  # fp32 with k > 512 on long rows takes the CTA path
@@ -72,7 +73,7 @@ def test_warp_rows_mixed_rows(dtype, length):
     """Consecutive rows of one warp differ in scale, offset and structure, so the
     carried threshold fails in both directions; ties, all-equal rows, ramps,
     signed zeros and subnormals force the sample retry and the exact fallback."""
-    b = _wr_batch()
+    b = _wr_batch(length)
     styles = ["normal", "ties", "allequal", "ramp", "signed_zero", "denormal"]
     per = b // len(styles) + 1
     parts = [workloads.random_rows(per, length, dtype, 900 + i, style=st)
@@ -92,7 +93,8 @@ def test_warp_rows_mixed_rows(dtype, length):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_warp_rows_causal_tail_and_nan(dtype):
     """c4-shaped rows (last quarter -inf) with NaN rows spread over the batch."""
-    b, n = _wr_batch(), 32768
+    n = 32768
+    b = _wr_batch(n)
     x = workloads.random_rows(b, n, dtype, 4242, style="normal")
     x[:, 3 * n // 4:] = float("-inf")
     for r in range(3, b, 97):
@@ -111,7 +113,8 @@ def test_warp_rows_causal_tail_and_nan(dtype):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_warp_rows_k_beyond_finite(dtype):
     """k larger than the finite count of a row: -inf elements are selected by index."""
-    b, n = _wr_batch(), 2048
+    n = 2048
+    b = _wr_batch(n)
     x = workloads.random_rows(b, n, dtype, 77, style="normal")
     x[:, 300:] = float("-inf")
     _assert_path(x, 512)
@@ -124,7 +127,7 @@ def test_warp_rows_ragged_stride(dtype):
     es = 2 if dtype == torch.bfloat16 else 4
     for length in (1001, 30001):
         stride = -(-(length + 5) * es // 16) * 16 // es
-        x = workloads.random_rows(_wr_batch(), length, dtype, 31, style="normal", row_stride=stride)
+        x = workloads.random_rows(_wr_batch(length), length, dtype, 31, style="normal", row_stride=stride)
         _assert_path(x, 100, length=length)
         gv, gi, gf = run_gpu(x, 100, True, True, length=length)
         assert gf == 0
@@ -134,7 +137,8 @@ def test_warp_rows_ragged_stride(dtype):
 def test_warp_rows_candidates_concentrated():
     """All of a row's large values in one short stretch (recent positions of an
     indexer row), in rows following ordinary rows."""
-    b, n = _wr_batch(), 32768
+    n = 32768
+    b = _wr_batch(n)
     x = workloads.random_rows(b, n, torch.bfloat16, 5150, style="normal")
     hot = torch.arange(b) % 2 == 1
     x[hot, n - 700:] = (x[hot, n - 700:].float() + 8.0).to(torch.bfloat16)
