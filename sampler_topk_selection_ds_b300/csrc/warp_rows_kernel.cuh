@@ -9,23 +9,25 @@
 // what hides HBM latency. Per row:
 //
 //  T  threshold t (an order key): the warp's previous row's k-th key lowered by
-//     a margin, or, for a warp's first row, a value read off a strided sample
-//     of vector maxima. t is only a guess; the step below checks it.
-//  S  stream the row once with coalesced 16-byte loads (vector v of the row is
-//     loaded by lane v mod 32); a vector whose NaN-propagating maximum reaches
-//     t is listed (ballot + popc, so the list stays in index order) and its
-//     data parked in a small shared-memory ring. Every 32 listed vectors the
-//     warp extracts their elements >= t (or NaN) as candidates, again in index
-//     order. The guess holds iff k <= candidates <= capacity: then the
-//     candidates contain the row's top k.
+//     a margin, or, for a warp's first row, a value read off a sample of vector
+//     maxima (16 evenly spaced blocks of 32 vectors). t is only a guess; the
+//     step below checks it.
+//  S  stream the row once through a per-warp shared-memory ring of 2 KB bulk
+//     async copies (lane v mod 32 reads vector v from it); a vector whose
+//     NaN-propagating maximum reaches t is listed (ballot + popc, so the list
+//     stays in index order) and its data parked in a small shared-memory ring.
+//     Every 32 listed vectors the warp extracts their elements >= t (or NaN) as
+//     candidates, again in index order. The guess holds iff k <= candidates <=
+//     capacity: then the candidates contain the row's top k.
 //  R  exact k-th key K* among the candidates: 256-bin histogram levels over
 //     the key range [t, max], each level narrowing the range by 8 bits.
 //  C  one ordered pass over the candidates: keep key > K*, and keys == K*
 //     while their running count stays below the ties still needed; outputs
 //     are written in ascending index order (sorted_index costs nothing).
 //
-// A row whose guess fails is retried with the sample threshold; a row that
-// still fails (massive ties, a NaN, k close to the row length) takes the exact
+// A row whose guess fails is retried (sample threshold, a sample rank adapted to
+// the count seen, the exact k-th vector maximum); a row that still fails
+// (massive ties, a NaN, k above the number of finite vectors) takes the exact
 // fallback: 8-bit radix levels over every element of the row, then one ordered
 // output pass. Rows with a NaN set the device flag there.
 //
