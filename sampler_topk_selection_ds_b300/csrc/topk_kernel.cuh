@@ -838,12 +838,21 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       return v < nfull ? ld_nc_v4(slice + v) : load_vec<ES>(rowp, v0 + v, p.len);
     };
     const int ncache = gv == 1 ? min(lc, p.lvec_cap) : 0;  // list entries held in wvec
-    if (gv == 1 && !vec_kept) {
+    // Every listed granule holds at least one candidate, so a CTA whose listed
+    // granules alone exceed the candidate capacity overflows for certain: it
+    // skips the counting pass (rows made of a few repeated values list most of
+    // their granules).
+    if (lane == 0) misc[kLcnt + warp] = static_cast<uint32_t>(lc);
+    __syncthreads();
+    uint32_t listed = 0;
+    for (int w = 0; w < kWarps; ++w) listed += misc[kLcnt + w];
+    const bool sure_over = listed > static_cast<uint32_t>(p.cand_cap);
+    if (gv == 1 && !vec_kept && !sure_over) {
       for (int j = lane; j < ncache; j += 32) wvec[j] = load_slice(wlist[j]);
       __syncwarp();
     }
     uint32_t wc = 0;
-    for (int j = lane; j < lc; j += 32) {
+    for (int j = lane; j < (sure_over ? 0 : lc); j += 32) {
       if (gv == 1) {
         const int v = wlist[j];
         const uint32_t m = vmask_of(v, j < ncache ? wvec[j] : load_slice(v));
@@ -856,10 +865,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       }
     }
     wc = warp_sum(wc);
-    if (lane == 0) {
-      wtot[kWarps + warp] = wc;
-      misc[kLcnt + warp] = static_cast<uint32_t>(lc);
-    }
+    if (lane == 0) wtot[kWarps + warp] = wc;
     __syncthreads();
     uint32_t cbase = 0, ncand = 0;
     for (int w = 0; w < kWarps; ++w) {
@@ -867,6 +873,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       if (w < warp) cbase += t;
       ncand += t;
     }
+    if (sure_over) ncand = listed;
     const bool cta_over = ncand > static_cast<uint32_t>(p.cand_cap);
     if (!cta_over) {
       // pass 2: write, lanes in index order; positions from ballots (almost every
@@ -1126,6 +1133,32 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       // ---- fallback: candidates did not fit; select over the listed granules, ------
       // re-read from global memory, with cluster-wide histograms.
       auto visit = [&](auto&& f) {
+        if (gv == 1) {  // 4 listed vectors in flight per lane (row vector indices fit 32 bits)
+          constexpr int UV = 4;
+          const int iv0 = static_cast<int>(v0), iv1 = static_cast<int>(v1), ilen = static_cast<int>(p.len);
+          for (int jb = 0; jb < lc; jb += 32 * UV) {
+            uint4 w[UV];
+            int v[UV];
+#pragma unroll
+            for (int u = 0; u < UV; ++u) {
+              const int j = jb + 32 * u + lane;
+              v[u] = j < lc ? iv0 + static_cast<int>(wlist[j]) : iv1;
+              w[u] = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
+              if (v[u] < iv1) w[u] = load_vec<ES>(rowp, v[u], p.len);
+            }
+#pragma unroll
+            for (int u = 0; u < UV; ++u) {
+              const bool vok = v[u] < iv1;
+#pragma unroll
+              for (int e = 0; e < VEC; ++e) {
+                const uint32_t eb = elem_bits<ES>(w[u], e);
+                const uint32_t key = key_of<ES>(eb);
+                f(key, vok && (v[u] * VEC + e < ilen) && (key >= T_full || is_nan_bits<ES>(eb)));
+              }
+            }
+          }
+          return;
+        }
         for (int j = lane; j < round_up32(lc); j += 32) {
           const bool gok = j < lc;
           for (int q = 0; q < gv; ++q) {
@@ -1231,8 +1264,11 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         base_gt += misc[kXpreGt];
         base_eq += misc[kXpreEq];
       }
-      // write pass: one granule per lane, lanes in index order
-      for (int j0 = 0; j0 < lc; j0 += 32) {
+      // write pass: one granule per lane, lanes in index order. Positions only
+      // grow from base_gt + min(base_eq, r_ties): when that is already k, this
+      // warp has nothing to write.
+      const bool none_here = base_gt + min(base_eq, r_ties) >= k;
+      for (int j0 = 0; j0 < (none_here ? 0 : lc); j0 += 32) {
         const int j = j0 + lane;
         const bool gok = j < lc;
         for (int q = 0; q < gv; ++q) {
