@@ -1268,48 +1268,71 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       // grow from base_gt + min(base_eq, r_ties): when that is already k, this
       // warp has nothing to write.
       const bool none_here = base_gt + min(base_eq, r_ties) >= k;
-      for (int j0 = 0; j0 < (none_here ? 0 : lc); j0 += 32) {
-        const int j = j0 + lane;
-        const bool gok = j < lc;
-        for (int q = 0; q < gv; ++q) {
-          const int64_t v = gok ? v0 + static_cast<int64_t>(wlist[j]) * gv + q : v1;
-          const bool vok = v < v1;
-          uint4 w = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
-          if (vok) w = load_vec<ES>(rowp, v, p.len);
-          uint32_t lg = 0, lq = 0;
+      // one vector per lane (vector v of the row, valid if vok), lanes in index order
+      auto write_vec = [&](const uint4& w, int64_t v, bool vok) {
+        uint32_t lg = 0, lq = 0;
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const uint32_t eb = elem_bits<ES>(w, e);
-            const uint32_t key = key_of<ES>(eb);
-            if (vok && v * VEC + e < p.len && (key >= T_full || is_nan_bits<ES>(eb))) {
-              lg += key > kstar;
-              lq += key == kstar;
+        for (int e = 0; e < VEC; ++e) {
+          const uint32_t eb = elem_bits<ES>(w, e);
+          const uint32_t key = key_of<ES>(eb);
+          if (vok && v * VEC + e < p.len && (key >= T_full || is_nan_bits<ES>(eb))) {
+            lg += key > kstar;
+            lq += key == kstar;
+          }
+        }
+        uint32_t bg = base_gt + warp_excl_scan(lg);
+        uint32_t bq = base_eq + warp_excl_scan(lq);
+        base_gt += warp_sum(lg);
+        base_eq += warp_sum(lq);
+        if (lg + lq == 0) return;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const int64_t idx = v * VEC + e;
+          const uint32_t bits = elem_bits<ES>(w, e);
+          const uint32_t key = key_of<ES>(bits);
+          if (vok && idx < p.len && (key >= T_full || is_nan_bits<ES>(bits))) {
+            uint32_t pos = 0xFFFFFFFFu;
+            if (key > kstar) {
+              pos = bg + min(bq, r_ties);
+              ++bg;
+            } else if (key == kstar) {
+              if (bq < r_ties) pos = bg + bq;
+              ++bq;
+            }
+            if (pos < k) {
+              out_idx[pos] = static_cast<int32_t>(idx);
+              if (out_val) out_val[pos] = static_cast<VT>(bits);
             }
           }
-          uint32_t bg = base_gt + warp_excl_scan(lg);
-          uint32_t bq = base_eq + warp_excl_scan(lq);
-          base_gt += warp_sum(lg);
-          base_eq += warp_sum(lq);
-          if (lg + lq == 0) continue;
+        }
+      };
+      if (gv == 1) {
+        // 4 listed vectors in flight per lane, handled in list order; stop once
+        // every later output would land at or beyond position k
+        constexpr int UV = 4;
+        for (int jb = 0; jb < (none_here ? 0 : lc); jb += 32 * UV) {
+          uint4 w[UV];
+          int64_t v[UV];
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const int64_t idx = v * VEC + e;
-            const uint32_t bits = elem_bits<ES>(w, e);
-            const uint32_t key = key_of<ES>(bits);
-            if (idx < p.len && (key >= T_full || is_nan_bits<ES>(bits))) {
-              uint32_t pos = 0xFFFFFFFFu;
-              if (key > kstar) {
-                pos = bg + min(bq, r_ties);
-                ++bg;
-              } else if (key == kstar) {
-                if (bq < r_ties) pos = bg + bq;
-                ++bq;
-              }
-              if (pos < k) {
-                out_idx[pos] = static_cast<int32_t>(idx);
-                if (out_val) out_val[pos] = static_cast<VT>(bits);
-              }
-            }
+          for (int u = 0; u < UV; ++u) {
+            const int j = jb + 32 * u + lane;
+            v[u] = j < lc ? v0 + static_cast<int64_t>(wlist[j]) : v1;
+            w[u] = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
+            if (v[u] < v1) w[u] = load_vec<ES>(rowp, v[u], p.len);
+          }
+#pragma unroll
+          for (int u = 0; u < UV; ++u) write_vec(w[u], v[u], v[u] < v1);
+          if (base_gt + min(base_eq, r_ties) >= k) break;
+        }
+      } else {
+        for (int j0 = 0; j0 < (none_here ? 0 : lc); j0 += 32) {
+          const int j = j0 + lane;
+          const bool gok = j < lc;
+          for (int q = 0; q < gv; ++q) {
+            const int64_t v = gok ? v0 + static_cast<int64_t>(wlist[j]) * gv + q : v1;
+            uint4 w = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
+            if (v < v1) w = load_vec<ES>(rowp, v, p.len);
+            write_vec(w, v, v < v1);
           }
         }
       }
