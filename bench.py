@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import dataclasses
 import glob
 import hashlib
 import io
@@ -317,6 +318,8 @@ def run_ours(args, w):
 
     bytes_step = w.bytes_in + w.bytes_out
     value = aggregate_value(bytes_step, args.steps, world, max_seconds)
+    launches = plan.launches + (1 if int(w.sorted_index) == 2 else 0)  # value order adds a sort
+    # one step's bytes over one step's device time (all of its launches)
     per_launch_s = seconds / (args.steps * plan.launches)
     achieved = bytes_step / plan.launches / per_launch_s / 1e9
     peak, peak_src = measured_peak()
@@ -345,7 +348,7 @@ def run_ours(args, w):
                          "kernel": kernel_name(w, plan),
                          "kernel_hash": kernel_hash()},
             "e2e": e2e,
-            "gpu_launches": args.steps * plan.launches,
+            "gpu_launches": args.steps * launches,
             "plan": plan.as_dict(),
             "clocks": clocks,
             "cpu_baseline": cb,
@@ -421,12 +424,16 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--order", default="workload", choices=["workload", "value"],
+                    help="value: ask for value-ordered output (sorted_index 2; one more launch per call)")
     ap.add_argument("--case", action="store_true",
                     help="profiling case: run the workload --calls times, untimed (for ncu)")
     ap.add_argument("--rows", type=int, default=0, help="--case: use only the first ROWS rows")
     ap.add_argument("--calls", type=int, default=3, help="--case: number of calls")
     args = ap.parse_args(argv)
     w = workloads.WORKLOADS[args.workload]
+    if args.order == "value":
+        w = dataclasses.replace(w, sorted_index=2)
     if args.case:
         return run_case(args, w)
     if args.impl == "reference":

@@ -64,6 +64,11 @@ typedef enum {
 /* Hard limit on k, from the pages ("topk <= 4096"). */
 #define DS_TOPK_MAX_K 4096
 
+/* Output order (the sorted_index argument). */
+#define DS_TOPK_SORT_NONE 0  /* unspecified order                                  */
+#define DS_TOPK_SORT_INDEX 1 /* ascending index                                    */
+#define DS_TOPK_SORT_VALUE 2 /* value descending, equal values by ascending index  */
+
 /*
  * ds_topk — batched row-wise TopK, enqueued on `stream`.
  *
@@ -81,10 +86,17 @@ typedef enum {
  *                row_stride * sizeof(dtype) must be a multiple of 16 bytes
  *                (the pages' "rows need a specific alignment, callers may pad").
  *   k            1 <= k <= min(len, DS_TOPK_MAX_K).
- *   sorted_index 0 or 1. 1: each output row lists its k indices in ascending
- *                index order. 0: the order within a row is unspecified (this
- *                implementation emits ascending index order in both modes,
+ *   sorted_index DS_TOPK_SORT_NONE (0), DS_TOPK_SORT_INDEX (1) or
+ *                DS_TOPK_SORT_VALUE (2). 1: each output row lists its k indices
+ *                in ascending index order. 0: the order within a row is
+ *                unspecified (this implementation emits ascending index order,
  *                because its ordered compaction produces it at no extra cost).
+ *                2: value descending, equal values by ascending index (the
+ *                selection's total order); this costs one more kernel launch on
+ *                the same stream, a per-row sort of the k outputs
+ *                (github-research.aiutil.com, "deepseek-ai/DeepSelect", section
+ *                关键技术亮点, item 2: outputs ordered by index or by value, either
+ *                at a cost in speed).
  *   return_value 0 or 1. 1: out_values[b*k + j] = the input bit pattern at
  *                column out_indices[b*k + j] (bitwise copy, -0.0 stays -0.0).
  *                0: out_values is not touched and may be NULL.
@@ -147,7 +159,8 @@ typedef struct {
   int64_t granules_per_cta;    /* size of the per-CTA granule-maximum array; on
                                   DS_TOPK_PATH_WARP_ROWS the candidate slots per warp  */
   int32_t smem_bytes;          /* dynamic shared memory per CTA                        */
-  int32_t launches;            /* kernel launches per call                             */
+  int32_t launches;            /* kernel launches per call with sorted_index 0 or 1
+                                  (DS_TOPK_SORT_VALUE adds one)                        */
 } ds_topk_plan_t;
 
 /*

@@ -62,12 +62,16 @@ def cores() -> int:
 
 
 def topk(x: torch.Tensor, k: int, length: Optional[int] = None, return_value: bool = True,
-         nthreads: int = 0, lib=None) -> Tuple[Optional[torch.Tensor], torch.Tensor, int, torch.Tensor]:
+         nthreads: int = 0, lib=None, order: str = "index") -> Tuple[Optional[torch.Tensor], torch.Tensor, int, torch.Tensor]:
     """Oracle TopK of a CPU tensor x [batch, row_stride] (bf16 or fp32).
 
-    Returns (values or None, indices int32 [batch,k] in ascending index order,
-    nan_flag int, row_nan bool [batch]). Rows holding a NaN get indices -1.
+    Returns (values or None, indices int32 [batch,k], nan_flag int, row_nan bool
+    [batch]). order="index": ascending index order; order="value": the total order
+    itself (value descending, equal values by ascending index). Rows holding a NaN
+    get indices -1.
     """
+    if order not in ("index", "value"):
+        raise ValueError(order)
     if x.device.type != "cpu":
         raise ValueError("the oracle runs on host memory only")
     if x.dtype not in (torch.bfloat16, torch.float32):
@@ -81,7 +85,8 @@ def topk(x: torch.Tensor, k: int, length: Optional[int] = None, return_value: bo
     flag = np.zeros(1, dtype=np.int32)
     row_nan = np.zeros(max(batch, 1), dtype=np.uint8)
     lib = lib or load()
-    rc = lib.oracle_topk(x.data_ptr(), dtype, batch, length, stride, k, 1, int(return_value),
+    rc = lib.oracle_topk(x.data_ptr(), dtype, batch, length, stride, k, 2 if order == "value" else 1,
+                         int(return_value),
                          vals.data_ptr() if vals is not None else None, idx.data_ptr(),
                          flag.ctypes.data, row_nan.ctypes.data, nthreads)
     if rc != 0:

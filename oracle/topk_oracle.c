@@ -86,6 +86,7 @@ typedef struct {
   int32_t* out_indices;
   uint8_t* row_nan;
   int64_t row_begin, row_end;
+  int by_value; /* 1: keep the first k pairs in the total order (value order) */
   int any_nan;
   int failed;
 } oracle_job;
@@ -117,7 +118,7 @@ static void select_rows(oracle_job* job) {
       continue;
     }
     qsort(pairs, (size_t)job->len, sizeof(oracle_pair), by_value_desc_index_asc);
-    qsort(pairs, (size_t)job->k, sizeof(oracle_pair), by_index_asc);
+    if (!job->by_value) qsort(pairs, (size_t)job->k, sizeof(oracle_pair), by_index_asc);
     for (int j = 0; j < job->k; ++j) {
       oi[j] = pairs[j].index;
       if (job->return_value) {
@@ -139,13 +140,17 @@ static void* run_job(void* arg) {
  * row_nan (optional, may be NULL) receives 1 for rows that hold a NaN.
  * nthreads <= 0 uses every online core. Returns 0, 1 on a bad argument, 2 on an
  * allocation or thread failure. *nan_flag gets bit 0 set if any row had a NaN
- * (never cleared). The output order is ascending index in both sorted_index modes.
+ * (never cleared). The output order is ascending index for sorted_index 0 and 1;
+ * for sorted_index 2 it is the total order itself (value descending, equal values
+ * by ascending index), as the first k pairs of the full sort come out
+ * (github-research.aiutil.com, "deepseek-ai/DeepSelect", section 关键技术亮点,
+ * item 2: outputs ordered by index or by value).
  */
 int oracle_topk(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
                 int k, int sorted_index, int return_value, void* out_values,
                 int32_t* out_indices, int32_t* nan_flag, uint8_t* row_nan, int nthreads) {
-  (void)sorted_index;
   if (dtype != 0 && dtype != 1) return 1;
+  if (sorted_index < 0 || sorted_index > 2) return 1;
   if (batch < 0 || len < 1 || len > INT32_MAX || row_stride < len) return 1;
   if (k < 1 || k > 4096 || (int64_t)k > len) return 1;
   if (batch == 0) return 0;
@@ -176,6 +181,7 @@ int oracle_topk(const void* x, int dtype, int64_t batch, int64_t len, int64_t ro
     j->out_values = out_values;
     j->out_indices = out_indices;
     j->row_nan = row_nan;
+    j->by_value = sorted_index == 2;
     j->row_begin = batch * t / nthreads;
     j->row_end = batch * (t + 1) / nthreads;
     if (nthreads == 1) {

@@ -26,6 +26,9 @@ MAX_K = 4096
 PATH_ROW = 0
 PATH_CLUSTER = 1
 PATH_WARP_ROWS = 2
+SORT_NONE = 0   # output order unspecified
+SORT_INDEX = 1  # ascending index
+SORT_VALUE = 2  # value descending, equal values by ascending index
 
 
 class Plan(ctypes.Structure):
@@ -97,13 +100,23 @@ def dtype_code(dt: torch.dtype) -> int:
     raise TypeError(f"ds_topk supports bfloat16 and float32 inputs, not {dt}")
 
 
-def topk(x: torch.Tensor, k: int, sorted_index: bool = False, return_value: bool = True,
+def _order_code(sorted_index) -> int:
+    if isinstance(sorted_index, str):
+        return {"none": SORT_NONE, "index": SORT_INDEX, "value": SORT_VALUE}[sorted_index]
+    if isinstance(sorted_index, bool):
+        return SORT_INDEX if sorted_index else SORT_NONE
+    return int(sorted_index)
+
+
+def topk(x: torch.Tensor, k: int, sorted_index=False, return_value: bool = True,
          length: Optional[int] = None, nan_flag: Optional[torch.Tensor] = None,
          out: Optional[Tuple[Optional[torch.Tensor], torch.Tensor]] = None,
          stream: Optional[torch.cuda.Stream] = None):
     """TopK of each row of a CUDA tensor x [batch, row_stride] (row stride may
     exceed `length`, the number of valid columns; padding is never read).
 
+    sorted_index: False/True (unspecified / ascending index), or "value"
+    (SORT_VALUE: value descending, equal values by ascending index).
     Returns (values or None, indices int32 [batch, k]). If nan_flag (an int32
     CUDA tensor with one element) is given, DS_TOPK_FLAG_NAN is OR-ed into it
     when a row holds a NaN; the caller clears it.
@@ -129,7 +142,7 @@ def topk(x: torch.Tensor, k: int, sorted_index: bool = False, return_value: bool
     flag = nan_flag if nan_flag is not None else torch.zeros(1, dtype=torch.int32, device=x.device)
     s = stream if stream is not None else torch.cuda.current_stream(x.device)
     rc = ds_topk(x.data_ptr(), dtype_code(x.dtype), batch, length, row_stride, k,
-                 int(bool(sorted_index)), int(bool(return_value)),
+                 _order_code(sorted_index), int(bool(return_value)),
                  vals.data_ptr() if (return_value and vals is not None) else None,
                  idx.data_ptr(), flag.data_ptr(), s.cuda_stream)
     if rc != OK:

@@ -16,6 +16,7 @@
 #include "ds_topk.h"
 #include "topk_kernel.cuh"
 #include "warp_rows_kernel.cuh"
+#include "value_order_kernel.cuh"
 
 namespace {
 
@@ -445,6 +446,59 @@ cudaError_t launch_dtype(const Plan& pl, cudaStream_t stream) {
 
 bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
 
+// sorted_index == DS_TOPK_SORT_VALUE: a second kernel on the same stream sorts
+// each row's k outputs by value (one CTA per row, a bitonic sort in shared
+// memory). It starts early through programmatic dependent launch and waits for
+// the selection kernel's outputs before reading them.
+template <int ES>
+cudaError_t launch_value_order(const char* x, int64_t batch, int64_t len, int64_t row_stride_bytes, int k,
+                               int return_value, void* out_values, int32_t* out_indices, int sm_count,
+                               cudaStream_t stream) {
+  ds_topk_dev::OrderParams op;
+  op.x = x;
+  op.batch = batch;
+  op.row_stride_bytes = row_stride_bytes;
+  op.len = len;
+  op.k = k;
+  int n2 = 64;  // one 64-word block per warp at least
+  while (n2 < k) n2 <<= 1;
+  op.n2 = n2;
+  op.return_value = return_value;
+  op.out_values = return_value ? out_values : nullptr;
+  op.out_indices = out_indices;
+  const int threads = n2 / 2 < 1024 ? n2 / 2 : 1024;  // n2 >= 64: at least one warp
+  const int64_t max_grid = static_cast<int64_t>(sm_count) * 16;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(batch < max_grid ? batch : max_grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(n2) * 8;  // <= 32 KB
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ds_topk_dev::topk_value_order_kernel<ES>, op);
+}
+
+// The optional value-order pass after a selection launch; DS_TOPK_OK or DS_TOPK_ECUDA.
+int finish_order(int es, int sorted_index, const void* x, int64_t batch, int64_t len, int64_t row_stride,
+                 int k, int return_value, void* out_values, int32_t* out_indices, int sm_count,
+                 cudaStream_t stream) {
+  if (sorted_index != DS_TOPK_SORT_VALUE) return DS_TOPK_OK;
+  const char* xb = static_cast<const char*>(x);
+  const cudaError_t e =
+      es == 2 ? launch_value_order<2>(xb, batch, len, row_stride * 2, k, return_value, out_values, out_indices,
+                                      sm_count, stream)
+              : launch_value_order<4>(xb, batch, len, row_stride * 4, k, return_value, out_values, out_indices,
+                                      sm_count, stream);
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) {
+    cudaGetLastError();
+    return DS_TOPK_ECUDA;
+  }
+  return DS_TOPK_OK;
+}
+
 }  // namespace
 
 extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
@@ -452,7 +506,8 @@ extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int
                        int32_t* out_indices, int32_t* nan_flag, cudaStream_t stream) {
   int rc = validate_sizes(dtype, batch, len, row_stride, k);
   if (rc != DS_TOPK_OK) return rc;
-  if ((sorted_index != 0 && sorted_index != 1) || (return_value != 0 && return_value != 1))
+  if (sorted_index < DS_TOPK_SORT_NONE || sorted_index > DS_TOPK_SORT_VALUE ||
+      (return_value != 0 && return_value != 1))
     return DS_TOPK_EINVAL;
   if (batch == 0) return DS_TOPK_OK;
   if (!x || !out_indices || !nan_flag || (return_value && !out_values)) return DS_TOPK_EINVAL;
@@ -484,7 +539,8 @@ extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int
       cudaGetLastError();
       return DS_TOPK_ECUDA;
     }
-    return DS_TOPK_OK;
+    return finish_order(es, sorted_index, x, batch, len, row_stride, k, return_value, out_values, out_indices,
+                        dev.sm_count, stream);
   }
   int resident = resident_cached(dev_id, pl, dev.sm_count);
   if (resident > 0 && batch > resident) {
@@ -514,7 +570,8 @@ extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int
     return DS_TOPK_ECUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return DS_TOPK_ECUDA;
-  return DS_TOPK_OK;
+  return finish_order(es, sorted_index, x, batch, len, row_stride, k, return_value, out_values, out_indices,
+                      dev.sm_count, stream);
 }
 
 extern "C" int ds_topk_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k,

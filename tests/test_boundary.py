@@ -52,7 +52,7 @@ P = 1 << 20  # a 16-byte-aligned fake address
     ((P, 0, 1, 16, 16, 0, 0, 1, P, P, P), dstk.EINVAL),          # k = 0
     ((P, 0, 1, 8192, 8192, 4097, 0, 1, P, P, P), dstk.EINVAL),   # k > 4096
     ((P, 0, 1, 16, 16, 17, 0, 1, P, P, P), dstk.EINVAL),         # k > len
-    ((P, 0, 1, 16, 16, 1, 2, 1, P, P, P), dstk.EINVAL),          # sorted_index not 0/1
+    ((P, 0, 1, 16, 16, 1, 3, 1, P, P, P), dstk.EINVAL),          # sorted_index not 0/1/2
     ((P, 0, 1, 16, 16, 1, 0, 3, P, P, P), dstk.EINVAL),          # return_value not 0/1
     ((0, 0, 1, 16, 16, 1, 0, 1, P, P, P), dstk.EINVAL),          # x NULL
     ((P, 0, 1, 16, 16, 1, 0, 1, P, 0, P), dstk.EINVAL),          # out_indices NULL

@@ -262,3 +262,31 @@ def test_planted_mistake_is_caught(mutant, tmp_path):
 
 def test_unmutated_oracle_passes_pin_subset():
     assert _all_pins_pass(oracle.load())
+
+
+# ---- value order (sorted_index = 2) ----------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("style", ["normal", "ties", "signed_zero", "denormal", "ramp"])
+def test_value_order_matches_stable_sort(dtype, style):
+    """Value order is the first k pairs of a stable descending sort: values
+    descending, equal values (including -0.0 and +0.0) by ascending index."""
+    x = workloads.random_rows(5, 333, dtype, 4711, style=style)
+    for k in (1, 7, 100, 333):
+        v, i, f, rn = oracle.topk(x, k, order="value")
+        assert f == 0
+        ref = torch.sort(x.to(torch.float64), dim=1, descending=True, stable=True)
+        assert torch.equal(i.to(torch.int64), ref.indices[:, :k])
+        assert np.array_equal(bits_of(v), bits_of(torch.gather(x, 1, i.to(torch.int64))))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_value_order_same_set_as_index_order(dtype):
+    x = workloads.random_rows(4, 2000, dtype, 99, style="normal")
+    x[1, 100:400] = 1.0  # a long run of equal values across the k-th position
+    for k in (64, 350, 2000):
+        vv, iv, _, _ = oracle.topk(x, k, order="value")
+        vi, ii, _, _ = oracle.topk(x, k, order="index")
+        assert torch.equal(torch.sort(iv, dim=1).values, ii)
+        keys = vv.to(torch.float64)
+        assert bool((keys[:, 1:] <= keys[:, :-1]).all())  # non-increasing values
