@@ -47,6 +47,10 @@ KERNEL_SOURCES = sorted(os.path.relpath(f, ROOT) for f in
                         glob.glob(os.path.join(ROOT, "sampler_topk_selection_ds_b300", "csrc", "*.cu*")))
 
 
+SAMPLE_TEMPERATURE = 1.0
+SAMPLE_TOP_P = 0.9
+
+
 def kernel_name(w, plan) -> str:
     es = 2 if w.dtype == torch.bfloat16 else 4
     if plan.path == 2:
@@ -263,11 +267,22 @@ def run_ours(args, w):
     rc, plan = dstk.ds_topk_plan(dt_code, w.batch, w.length, w.length, w.k, props.multi_processor_count)
     assert rc == dstk.OK, dstk.status_string(rc)
 
+    sampling = args.order == "sample"
+    if sampling:  # the sampler tail needs the values; one fixed uniform number per row
+        vals = torch.empty((w.batch, w.k), dtype=w.dtype, device=dev)
+        u_dev = torch.rand(w.batch, generator=torch.Generator().manual_seed(w.seed)).to(dev)
+        tokens = torch.empty(w.batch, dtype=torch.int32, device=dev)
+
     def step(i, stream):
-        r = dstk.ds_topk(xs[i % copies].data_ptr(), dt_code, w.batch, w.length, w.length, w.k,
-                         int(w.sorted_index), int(w.return_value),
-                         vals.data_ptr() if vals is not None else None, idx.data_ptr(),
-                         flag.data_ptr(), stream.cuda_stream)
+        if sampling:
+            r = dstk.ds_topk_sample(xs[i % copies].data_ptr(), dt_code, w.batch, w.length, w.length, w.k,
+                                    SAMPLE_TEMPERATURE, SAMPLE_TOP_P, u_dev.data_ptr(), vals.data_ptr(),
+                                    idx.data_ptr(), tokens.data_ptr(), flag.data_ptr(), stream.cuda_stream)
+        else:
+            r = dstk.ds_topk(xs[i % copies].data_ptr(), dt_code, w.batch, w.length, w.length, w.k,
+                             int(w.sorted_index), int(w.return_value),
+                             vals.data_ptr() if vals is not None else None, idx.data_ptr(),
+                             flag.data_ptr(), stream.cuda_stream)
         if r != dstk.OK:
             raise dstk.DsTopkError(r)
 
@@ -318,7 +333,8 @@ def run_ours(args, w):
 
     bytes_step = w.bytes_in + w.bytes_out
     value = aggregate_value(bytes_step, args.steps, world, max_seconds)
-    launches = plan.launches + (1 if int(w.sorted_index) == 2 else 0)  # value order adds a sort
+    # value order adds a sort, the sampler tail a draw
+    launches = plan.launches + (1 if int(w.sorted_index) == 2 else 0) + (1 if sampling else 0)
     # one step's bytes over one step's device time (all of its launches)
     per_launch_s = seconds / (args.steps * plan.launches)
     achieved = bytes_step / plan.launches / per_launch_s / 1e9
@@ -339,7 +355,8 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "u16" if w.dtype == torch.bfloat16 else "u32",
             "data": "synthetic (seeded SplitMix64 + Box-Muller, workloads.py)",
-            "config": _config(w, l2_note),
+            "config": dict(_config(w, l2_note), **({"call": f"ds_topk_sample (temperature {SAMPLE_TEMPERATURE}, "
+                                                           f"top_p {SAMPLE_TOP_P})"} if sampling else {})),
             "rows_per_s": round(w.batch * args.steps * world / max_seconds, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -424,16 +441,18 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--order", default="workload", choices=["workload", "value"],
-                    help="value: ask for value-ordered output (sorted_index 2; one more launch per call)")
+    ap.add_argument("--order", default="workload", choices=["workload", "value", "sample"],
+                    help="value: value-ordered output (sorted_index 2; one more launch per call); "
+                         "sample: the sampler tail ds_topk_sample (temperature 1, top_p 0.9; "
+                         "three launches per call)")
     ap.add_argument("--case", action="store_true",
                     help="profiling case: run the workload --calls times, untimed (for ncu)")
     ap.add_argument("--rows", type=int, default=0, help="--case: use only the first ROWS rows")
     ap.add_argument("--calls", type=int, default=3, help="--case: number of calls")
     args = ap.parse_args(argv)
     w = workloads.WORKLOADS[args.workload]
-    if args.order == "value":
-        w = dataclasses.replace(w, sorted_index=2)
+    if args.order in ("value", "sample"):
+        w = dataclasses.replace(w, sorted_index=2, return_value=True)
     if args.case:
         return run_case(args, w)
     if args.impl == "reference":

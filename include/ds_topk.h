@@ -135,6 +135,45 @@ DS_TOPK_API int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, in
             int k, int sorted_index, int return_value, void* out_values,
             int32_t* out_indices, int32_t* nan_flag, cudaStream_t stream);
 
+/*
+ * ds_topk_sample — the sampler tail after TopK: for each row, select the k
+ * largest logits in value order (as ds_topk with sorted_index =
+ * DS_TOPK_SORT_VALUE and return_value = 1, into out_values / out_indices), then
+ * draw one column from them:
+ *   w_j = exp((v_j - v_0) / temperature)  over the k survivors in value order
+ *         (v_0 the largest; if v_0 is +inf, the +inf values weigh 1, the rest 0),
+ *   C_j = w_0 + ... + w_j, the nucleus is the shortest prefix [0, m] with
+ *   C_m >= top_p * C_{k-1}, and the token is the column at the first j <= m with
+ *   C_j > u[b] * C_m (inverse CDF).
+ * github-research.aiutil.com, "deepseek-ai/DeepSelect", section 关键技术亮点: the
+ * sampler path of TopK, whose survivors the next token is drawn from;
+ * deepseek.csdn.net, "DeepSeek 一次开源三个仓库": temperature and top_p as the
+ * request's sampling parameters. Readings where the pages are silent: the
+ * softmax runs over the k survivors only; top-p keeps the shortest prefix that
+ * reaches the mass; the draw takes the caller's uniform number.
+ *
+ * Arguments: x, dtype, batch, len, row_stride, k, nan_flag and stream as for
+ * ds_topk.
+ *   temperature  finite, > 0.
+ *   top_p        0 < top_p <= 1.
+ *   u            device pointer [batch] float, each in [0, 1), 4-byte aligned:
+ *                one uniform random number per row (the caller draws them).
+ *   out_values   device pointer [batch, k] of `dtype` (required): the k
+ *                selected values in value order.
+ *   out_indices  device pointer [batch, k] int32: their columns.
+ *   out_tokens   device pointer [batch] int32, 4-byte aligned: the drawn column.
+ * The arithmetic is fp32 (expf and sums over the k survivors); a draw can
+ * differ from an exact (float64) computation only when u * C_m or
+ * top_p * C_{k-1} lies within about (k + 2) * 2^-23 * C_{k-1} of a step of C.
+ * A row holding a NaN gets an unspecified but in-range token.
+ * Returns DS_TOPK_OK, DS_TOPK_EINVAL (also for a bad temperature or top_p),
+ * DS_TOPK_EALIGN or DS_TOPK_ECUDA, like ds_topk; nothing is enqueued on an
+ * argument error. Three kernel launches on `stream`; no allocation.
+ */
+DS_TOPK_API int ds_topk_sample(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
+                   int k, float temperature, float top_p, const float* u, void* out_values,
+                   int32_t* out_indices, int32_t* out_tokens, int32_t* nan_flag, cudaStream_t stream);
+
 /* Which kernel family a call runs. */
 typedef enum {
   DS_TOPK_PATH_ROW = 0,      /* one CTA per row                                     */

@@ -56,6 +56,11 @@ def _load() -> ctypes.CDLL:
     lib.ds_topk.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                             ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    lib.ds_topk_sample.restype = ctypes.c_int
+    lib.ds_topk_sample.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                   ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_void_p]
     lib.ds_topk_plan.restype = ctypes.c_int
     lib.ds_topk_plan.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                  ctypes.c_int, ctypes.c_int, ctypes.POINTER(Plan)]
@@ -83,6 +88,14 @@ def ds_topk(x: int, dtype: int, batch: int, length: int, row_stride: int, k: int
     """The C call, verbatim: pointers and the stream are plain integers."""
     return int(lib.ds_topk(x, dtype, batch, length, row_stride, k, sorted_index, return_value,
                            out_values, out_indices, nan_flag, stream))
+
+
+def ds_topk_sample(x: int, dtype: int, batch: int, length: int, row_stride: int, k: int,
+                   temperature: float, top_p: float, u: int, out_values: int, out_indices: int,
+                   out_tokens: int, nan_flag: int, stream: int = 0) -> int:
+    """The C call, verbatim: pointers and the stream are plain integers."""
+    return int(lib.ds_topk_sample(x, dtype, batch, length, row_stride, k, temperature, top_p, u,
+                                  out_values, out_indices, out_tokens, nan_flag, stream))
 
 
 def ds_topk_plan(dtype: int, batch: int, length: int, row_stride: int, k: int,
@@ -148,3 +161,29 @@ def topk(x: torch.Tensor, k: int, sorted_index=False, return_value: bool = True,
     if rc != OK:
         raise DsTopkError(rc)
     return vals, idx
+
+
+def sample(x: torch.Tensor, k: int, temperature: float, top_p: float, u: torch.Tensor,
+           nan_flag: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """Sampler tail on a CUDA tensor x [batch, len] (contiguous rows, 16-byte row
+    stride): TopK in value order, temperature softmax over the k survivors, top-p
+    nucleus, one draw per row with the caller's uniform numbers u (float32 CUDA
+    [batch], each in [0, 1)). Returns (tokens int32 [batch], values [batch, k],
+    indices int32 [batch, k])."""
+    if x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D CUDA tensor with contiguous rows")
+    if u.dtype != torch.float32 or not u.is_cuda or u.numel() != x.shape[0]:
+        raise ValueError("u must be a float32 CUDA tensor with one number per row")
+    batch, length = x.shape
+    row_stride = x.stride(0) if batch > 1 else -(-length * x.element_size() // 16) * 16 // x.element_size()
+    vals = torch.empty((batch, k), dtype=x.dtype, device=x.device)
+    idx = torch.empty((batch, k), dtype=torch.int32, device=x.device)
+    tokens = torch.empty(batch, dtype=torch.int32, device=x.device)
+    flag = nan_flag if nan_flag is not None else torch.zeros(1, dtype=torch.int32, device=x.device)
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    rc = ds_topk_sample(x.data_ptr(), dtype_code(x.dtype), batch, length, row_stride, k,
+                        float(temperature), float(top_p), u.contiguous().data_ptr(), vals.data_ptr(),
+                        idx.data_ptr(), tokens.data_ptr(), flag.data_ptr(), s.cuda_stream)
+    if rc != OK:
+        raise DsTopkError(rc)
+    return tokens, vals, idx

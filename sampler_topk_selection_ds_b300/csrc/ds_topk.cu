@@ -10,6 +10,7 @@
 // CTAs share one row from those sizes and the SM count.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -17,6 +18,7 @@
 #include "topk_kernel.cuh"
 #include "warp_rows_kernel.cuh"
 #include "value_order_kernel.cuh"
+#include "sampler_kernel.cuh"
 
 namespace {
 
@@ -572,6 +574,53 @@ extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int
   if (cudaGetLastError() != cudaSuccess) return DS_TOPK_ECUDA;
   return finish_order(es, sorted_index, x, batch, len, row_stride, k, return_value, out_values, out_indices,
                       dev.sm_count, stream);
+}
+
+extern "C" int ds_topk_sample(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
+                              int k, float temperature, float top_p, const float* u, void* out_values,
+                              int32_t* out_indices, int32_t* out_tokens, int32_t* nan_flag,
+                              cudaStream_t stream) {
+  if (!(temperature > 0.f) || !std::isfinite(temperature) || !(top_p > 0.f) || !(top_p <= 1.f))
+    return DS_TOPK_EINVAL;
+  int rc = validate_sizes(dtype, batch, len, row_stride, k);
+  if (rc != DS_TOPK_OK) return rc;
+  if (batch == 0) return DS_TOPK_OK;
+  if (!u || !out_tokens || !out_values) return DS_TOPK_EINVAL;
+  if (misaligned(u, 4) || misaligned(out_tokens, 4)) return DS_TOPK_EALIGN;
+  // the k survivors in value order, with their values
+  rc = ds_topk(x, dtype, batch, len, row_stride, k, DS_TOPK_SORT_VALUE, 1, out_values, out_indices, nan_flag,
+               stream);
+  if (rc != DS_TOPK_OK) return rc;
+  DeviceInfo dev;
+  rc = device_info(&dev);
+  if (rc != DS_TOPK_OK) return rc;
+  ds_topk_dev::SampleParams sp;
+  sp.batch = batch;
+  sp.k = k;
+  sp.inv_temperature = 1.0f / temperature;
+  sp.top_p = top_p;
+  sp.u = u;
+  sp.values = out_values;
+  sp.indices = out_indices;
+  sp.tokens = out_tokens;
+  const int64_t max_grid = static_cast<int64_t>(dev.sm_count) * 8;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(batch < max_grid ? batch : max_grid), 1, 1);
+  cfg.blockDim = dim3(ds_topk_dev::kSampleThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = dtype == DS_TOPK_BF16 ? cudaLaunchKernelEx(&cfg, ds_topk_dev::topk_sample_kernel<2>, sp)
+                                              : cudaLaunchKernelEx(&cfg, ds_topk_dev::topk_sample_kernel<4>, sp);
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) {
+    cudaGetLastError();
+    return DS_TOPK_ECUDA;
+  }
+  return DS_TOPK_OK;
 }
 
 extern "C" int ds_topk_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k,
