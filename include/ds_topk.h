@@ -64,6 +64,10 @@ typedef enum {
 /* Hard limit on k, from the pages ("topk <= 4096"). */
 #define DS_TOPK_MAX_K 4096
 
+/* Index type of out_indices (the index_type argument of ds_topk_ex). */
+#define DS_TOPK_INDEX_INT32 0
+#define DS_TOPK_INDEX_INT64 1
+
 /* Output order (the sorted_index argument). */
 #define DS_TOPK_SORT_NONE 0  /* unspecified order                                  */
 #define DS_TOPK_SORT_INDEX 1 /* ascending index                                    */
@@ -134,6 +138,18 @@ typedef enum {
 DS_TOPK_API int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
             int k, int sorted_index, int return_value, void* out_values,
             int32_t* out_indices, int32_t* nan_flag, cudaStream_t stream);
+
+/*
+ * ds_topk_ex — ds_topk with a selectable index type (deepseek.csdn.net,
+ * "DeepSeek 一次开源三个仓库", section 三: the call's indices_type argument).
+ * index_type DS_TOPK_INDEX_INT32: out_indices is int32 [batch, k] (4-byte
+ * aligned), exactly ds_topk; DS_TOPK_INDEX_INT64: out_indices is int64
+ * [batch, k], 8-byte aligned. Everything else as ds_topk; any other index_type
+ * returns DS_TOPK_EINVAL with nothing enqueued.
+ */
+DS_TOPK_API int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
+               int k, int sorted_index, int return_value, int index_type, void* out_values,
+               void* out_indices, int32_t* nan_flag, cudaStream_t stream);
 
 /*
  * ds_topk_sample — the sampler tail after TopK: for each row, select the k

@@ -26,6 +26,8 @@ MAX_K = 4096
 PATH_ROW = 0
 PATH_CLUSTER = 1
 PATH_WARP_ROWS = 2
+INDEX_INT32 = 0
+INDEX_INT64 = 1
 SORT_NONE = 0   # output order unspecified
 SORT_INDEX = 1  # ascending index
 SORT_VALUE = 2  # value descending, equal values by ascending index
@@ -56,6 +58,10 @@ def _load() -> ctypes.CDLL:
     lib.ds_topk.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                             ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    lib.ds_topk_ex.restype = ctypes.c_int
+    lib.ds_topk_ex.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                               ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     lib.ds_topk_sample.restype = ctypes.c_int
     lib.ds_topk_sample.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_float,
@@ -88,6 +94,14 @@ def ds_topk(x: int, dtype: int, batch: int, length: int, row_stride: int, k: int
     """The C call, verbatim: pointers and the stream are plain integers."""
     return int(lib.ds_topk(x, dtype, batch, length, row_stride, k, sorted_index, return_value,
                            out_values, out_indices, nan_flag, stream))
+
+
+def ds_topk_ex(x: int, dtype: int, batch: int, length: int, row_stride: int, k: int,
+               sorted_index: int, return_value: int, index_type: int, out_values: Optional[int],
+               out_indices: int, nan_flag: int, stream: int = 0) -> int:
+    """The C call, verbatim: pointers and the stream are plain integers."""
+    return int(lib.ds_topk_ex(x, dtype, batch, length, row_stride, k, sorted_index, return_value,
+                              index_type, out_values, out_indices, nan_flag, stream))
 
 
 def ds_topk_sample(x: int, dtype: int, batch: int, length: int, row_stride: int, k: int,
@@ -124,13 +138,14 @@ def _order_code(sorted_index) -> int:
 def topk(x: torch.Tensor, k: int, sorted_index=False, return_value: bool = True,
          length: Optional[int] = None, nan_flag: Optional[torch.Tensor] = None,
          out: Optional[Tuple[Optional[torch.Tensor], torch.Tensor]] = None,
-         stream: Optional[torch.cuda.Stream] = None):
+         stream: Optional[torch.cuda.Stream] = None, index_dtype: torch.dtype = torch.int32):
     """TopK of each row of a CUDA tensor x [batch, row_stride] (row stride may
     exceed `length`, the number of valid columns; padding is never read).
 
     sorted_index: False/True (unspecified / ascending index), or "value"
     (SORT_VALUE: value descending, equal values by ascending index).
-    Returns (values or None, indices int32 [batch, k]). If nan_flag (an int32
+    index_dtype: torch.int32 (ds_topk) or torch.int64 (ds_topk_ex, INDEX_INT64).
+    Returns (values or None, indices [batch, k]). If nan_flag (an int32
     CUDA tensor with one element) is given, DS_TOPK_FLAG_NAN is OR-ed into it
     when a row holds a NaN; the caller clears it.
     """
@@ -148,16 +163,19 @@ def topk(x: torch.Tensor, k: int, sorted_index=False, return_value: bool = True,
         es = x.element_size()
         row_stride = -(-max(length, 1) * es // 16) * 16 // es
     if out is None:
-        idx = torch.empty((batch, k), dtype=torch.int32, device=x.device)
+        idx = torch.empty((batch, k), dtype=index_dtype, device=x.device)
         vals = torch.empty((batch, k), dtype=x.dtype, device=x.device) if return_value else None
     else:
         vals, idx = out
     flag = nan_flag if nan_flag is not None else torch.zeros(1, dtype=torch.int32, device=x.device)
     s = stream if stream is not None else torch.cuda.current_stream(x.device)
-    rc = ds_topk(x.data_ptr(), dtype_code(x.dtype), batch, length, row_stride, k,
-                 _order_code(sorted_index), int(bool(return_value)),
-                 vals.data_ptr() if (return_value and vals is not None) else None,
-                 idx.data_ptr(), flag.data_ptr(), s.cuda_stream)
+    if index_dtype not in (torch.int32, torch.int64) or idx.dtype != index_dtype:
+        raise ValueError("indices are int32 or int64, matching index_dtype")
+    rc = ds_topk_ex(x.data_ptr(), dtype_code(x.dtype), batch, length, row_stride, k,
+                    _order_code(sorted_index), int(bool(return_value)),
+                    INDEX_INT64 if index_dtype == torch.int64 else INDEX_INT32,
+                    vals.data_ptr() if (return_value and vals is not None) else None,
+                    idx.data_ptr(), flag.data_ptr(), s.cuda_stream)
     if rc != OK:
         raise DsTopkError(rc)
     return vals, idx

@@ -129,6 +129,7 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
       w.return_value = 0;
       w.out_values = nullptr;
       w.out_indices = nullptr;
+      w.idx64 = 0;
       w.flag = nullptr;
       return DS_TOPK_OK;
     }
@@ -223,6 +224,7 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
   p.return_value = 0;
   p.out_values = nullptr;
   p.out_indices = nullptr;
+  p.idx64 = 0;
   p.flag = nullptr;
   return DS_TOPK_OK;
 }
@@ -454,8 +456,8 @@ bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t
 // the selection kernel's outputs before reading them.
 template <int ES>
 cudaError_t launch_value_order(const char* x, int64_t batch, int64_t len, int64_t row_stride_bytes, int k,
-                               int return_value, void* out_values, int32_t* out_indices, int sm_count,
-                               cudaStream_t stream) {
+                               int return_value, void* out_values, void* out_indices, int idx64,
+                               int sm_count, cudaStream_t stream) {
   ds_topk_dev::OrderParams op;
   op.x = x;
   op.batch = batch;
@@ -468,6 +470,7 @@ cudaError_t launch_value_order(const char* x, int64_t batch, int64_t len, int64_
   op.return_value = return_value;
   op.out_values = return_value ? out_values : nullptr;
   op.out_indices = out_indices;
+  op.idx64 = idx64;
   const int threads = n2 / 2 < 1024 ? n2 / 2 : 1024;  // n2 >= 64: at least one warp
   const int64_t max_grid = static_cast<int64_t>(sm_count) * 16;
   cudaLaunchConfig_t cfg = {};
@@ -485,15 +488,15 @@ cudaError_t launch_value_order(const char* x, int64_t batch, int64_t len, int64_
 
 // The optional value-order pass after a selection launch; DS_TOPK_OK or DS_TOPK_ECUDA.
 int finish_order(int es, int sorted_index, const void* x, int64_t batch, int64_t len, int64_t row_stride,
-                 int k, int return_value, void* out_values, int32_t* out_indices, int sm_count,
+                 int k, int return_value, void* out_values, void* out_indices, int idx64, int sm_count,
                  cudaStream_t stream) {
   if (sorted_index != DS_TOPK_SORT_VALUE) return DS_TOPK_OK;
   const char* xb = static_cast<const char*>(x);
   const cudaError_t e =
       es == 2 ? launch_value_order<2>(xb, batch, len, row_stride * 2, k, return_value, out_values, out_indices,
-                                      sm_count, stream)
+                                      idx64, sm_count, stream)
               : launch_value_order<4>(xb, batch, len, row_stride * 4, k, return_value, out_values, out_indices,
-                                      sm_count, stream);
+                                      idx64, sm_count, stream);
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) {
     cudaGetLastError();
     return DS_TOPK_ECUDA;
@@ -503,18 +506,20 @@ int finish_order(int es, int sorted_index, const void* x, int64_t batch, int64_t
 
 }  // namespace
 
-extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
-                       int k, int sorted_index, int return_value, void* out_values,
-                       int32_t* out_indices, int32_t* nan_flag, cudaStream_t stream) {
+extern "C" int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
+                          int k, int sorted_index, int return_value, int index_type, void* out_values,
+                          void* out_indices, int32_t* nan_flag, cudaStream_t stream) {
   int rc = validate_sizes(dtype, batch, len, row_stride, k);
   if (rc != DS_TOPK_OK) return rc;
   if (sorted_index < DS_TOPK_SORT_NONE || sorted_index > DS_TOPK_SORT_VALUE ||
-      (return_value != 0 && return_value != 1))
+      (return_value != 0 && return_value != 1) ||
+      (index_type != DS_TOPK_INDEX_INT32 && index_type != DS_TOPK_INDEX_INT64))
     return DS_TOPK_EINVAL;
   if (batch == 0) return DS_TOPK_OK;
   if (!x || !out_indices || !nan_flag || (return_value && !out_values)) return DS_TOPK_EINVAL;
   const int es = dtype == DS_TOPK_BF16 ? 2 : 4;
-  if (misaligned(x, 16) || misaligned(out_indices, 4) || misaligned(nan_flag, 4) ||
+  const int idx64 = index_type == DS_TOPK_INDEX_INT64 ? 1 : 0;
+  if (misaligned(x, 16) || misaligned(out_indices, idx64 ? 8 : 4) || misaligned(nan_flag, 4) ||
       (return_value && misaligned(out_values, es)))
     return DS_TOPK_EALIGN;
 
@@ -533,6 +538,7 @@ extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int
     pl.wprm.return_value = return_value;
     pl.wprm.out_values = return_value ? out_values : nullptr;
     pl.wprm.out_indices = out_indices;
+    pl.wprm.idx64 = idx64;
     pl.wprm.flag = nan_flag;
     const int resident_ctas = resident_cached(dev_id, pl, dev.sm_count);
     if (resident_ctas > 0 && pl.pub.grid_ctas > resident_ctas) pl.pub.grid_ctas = resident_ctas;
@@ -542,7 +548,7 @@ extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int
       return DS_TOPK_ECUDA;
     }
     return finish_order(es, sorted_index, x, batch, len, row_stride, k, return_value, out_values, out_indices,
-                        dev.sm_count, stream);
+                        idx64, dev.sm_count, stream);
   }
   int resident = resident_cached(dev_id, pl, dev.sm_count);
   if (resident > 0 && batch > resident) {
@@ -561,6 +567,7 @@ extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int
   pl.prm.return_value = return_value;
   pl.prm.out_values = return_value ? out_values : nullptr;
   pl.prm.out_indices = out_indices;
+  pl.prm.idx64 = idx64;
   pl.prm.flag = nan_flag;
   // Persistent launch: no more clusters than can be resident at once; each one
   // walks the rows with a stride (and reuses its threshold from row to row).
@@ -573,7 +580,14 @@ extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int
   }
   if (cudaGetLastError() != cudaSuccess) return DS_TOPK_ECUDA;
   return finish_order(es, sorted_index, x, batch, len, row_stride, k, return_value, out_values, out_indices,
-                      dev.sm_count, stream);
+                      idx64, dev.sm_count, stream);
+}
+
+extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride, int k,
+                       int sorted_index, int return_value, void* out_values, int32_t* out_indices,
+                       int32_t* nan_flag, cudaStream_t stream) {
+  return ds_topk_ex(x, dtype, batch, len, row_stride, k, sorted_index, return_value, DS_TOPK_INDEX_INT32,
+                    out_values, out_indices, nan_flag, stream);
 }
 
 extern "C" int ds_topk_sample(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,

@@ -71,7 +71,8 @@ struct Params {
   int32_t k;
   int32_t return_value;
   void* out_values;
-  int32_t* out_indices;
+  void* out_indices;     // int32 or int64 (idx64)
+  int32_t idx64;
   int32_t* flag;
 };
 
@@ -203,6 +204,15 @@ __device__ __forceinline__ int round_up32(int n) { return (n + 31) & ~31; }
 // boundary (values spread over many bins) or over the few candidates of a row.
 __device__ __forceinline__ void hist_add(uint32_t* h, uint32_t digit, bool valid) {
   if (valid) atomicAdd(&h[digit], 1u);
+}
+
+// Output index store and load: int32, or int64 when the caller asked for it.
+__device__ __forceinline__ void put_index(void* out, int64_t pos, int64_t idx, int32_t idx64) {
+  if (idx64) static_cast<int64_t*>(out)[pos] = idx;
+  else static_cast<int32_t*>(out)[pos] = static_cast<int32_t>(idx);
+}
+__device__ __forceinline__ int64_t get_index(const void* out, int64_t pos, int32_t idx64) {
+  return idx64 ? static_cast<const int64_t*>(out)[pos] : static_cast<int64_t>(static_cast<const int32_t*>(out)[pos]);
 }
 
 // Load a u32 from the same shared-memory offset in cluster CTA `rank`.
@@ -986,7 +996,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       }
     }
 
-    int32_t* out_idx = p.out_indices + row * static_cast<int64_t>(k);
+    const int64_t out_base = row * static_cast<int64_t>(k);  // this row's first output
     VT* out_val = p.return_value ? reinterpret_cast<VT*>(p.out_values) + row * static_cast<int64_t>(k) : nullptr;
 
     if (dense && work_here) {
@@ -1125,7 +1135,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         if ((mg >> lane) & 1u) pos = bg + min(bq, r_ties);
         else if (((mq >> lane) & 1u) && bq < r_ties) pos = bg + bq;
         if (pos < k) {
-          out_idx[pos] = static_cast<int32_t>(c1[sbase + c]);
+          put_index(p.out_indices, out_base + pos, c1[sbase + c], p.idx64);
           if (out_val) out_val[pos] = static_cast<VT>(cand_bits<ES>(w0));
         }
       }
@@ -1300,7 +1310,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
               ++bq;
             }
             if (pos < k) {
-              out_idx[pos] = static_cast<int32_t>(idx);
+              put_index(p.out_indices, out_base + pos, idx, p.idx64);
               if (out_val) out_val[pos] = static_cast<VT>(bits);
             }
           }

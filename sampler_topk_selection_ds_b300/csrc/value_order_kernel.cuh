@@ -31,7 +31,8 @@ struct OrderParams {
   int32_t n2;  // k rounded up to a power of two, at least 64 (sort width)
   int32_t return_value;
   void* out_values;
-  int32_t* out_indices;
+  void* out_indices;  // int32 or int64 (idx64)
+  int32_t idx64;
 };
 
 template <int ES>
@@ -85,12 +86,12 @@ __global__ void __launch_bounds__(1024) topk_value_order_kernel(const OrderParam
   using VT = typename std::conditional<ES == 2, uint16_t, uint32_t>::type;
   for (int64_t row = blockIdx.x; row < p.batch; row += gridDim.x) {
     const char* rowp = p.x + row * p.row_stride_bytes;
-    int32_t* oi = p.out_indices + row * static_cast<int64_t>(p.k);
+    const int64_t ob = row * static_cast<int64_t>(p.k);
     VT* ov = p.return_value ? static_cast<VT*>(p.out_values) + row * static_cast<int64_t>(p.k) : nullptr;
     for (int j = tid; j < n2; j += nt) {
       unsigned long long w = 0ull;  // padding sorts last
       if (j < p.k) {
-        int64_t idx = oi[j];
+        int64_t idx = get_index(p.out_indices, ob + j, p.idx64);
         if (idx < 0 || idx >= p.len) idx = 0;  // never read outside the row
         // values already written by the selection are read in order; else gather
         const uint32_t bits = ov ? static_cast<uint32_t>(ov[j]) : load_bits<ES>(rowp, idx);
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(1024) topk_value_order_kernel(const OrderParam
     for (int j = tid; j < p.k; j += nt) {
       const unsigned long long w = sw[j];
       const uint32_t idx = 0xFFFFFFFFu - static_cast<uint32_t>(w);
-      oi[j] = static_cast<int32_t>(idx);
+      put_index(p.out_indices, ob + j, idx, p.idx64);
       if (ov) {
         uint32_t bits;
         if (!bits_of_key<ES>(static_cast<uint32_t>(w >> 32), &bits)) bits = load_bits<ES>(rowp, idx);

@@ -68,7 +68,8 @@ struct WrParams {
   int32_t k;
   int32_t return_value;
   void* out_values;
-  int32_t* out_indices;
+  void* out_indices;      // int32 or int64 (idx64)
+  int32_t idx64;
   int32_t* flag;
 };
 
@@ -577,7 +578,7 @@ struct WarpRow {
       const uint32_t sb = __ballot_sync(kFull, sel);
       if (sel && out + __popc(sb & lt) < p.k) {
         const int64_t o = obase + out + __popc(sb & lt);
-        p.out_indices[o] = idx_at(j);
+        put_index(p.out_indices, o, idx_at(j), p.idx64);
         if (p.return_value) {
           if constexpr (ES == 2) static_cast<uint16_t*>(p.out_values)[o] = static_cast<uint16_t>(bits);
           else static_cast<uint32_t*>(p.out_values)[o] = bits;
@@ -688,7 +689,7 @@ struct WarpRow {
       while (msel && o < obase + p.k) {
         const int e = __ffs(msel) - 1;
         msel &= msel - 1;
-        p.out_indices[o] = v * VEC + e;
+        put_index(p.out_indices, o, v * VEC + e, p.idx64);
         if (p.return_value) {
           const uint32_t bits = elem_bits<ES>(w, e);
           if constexpr (ES == 2) static_cast<uint16_t*>(p.out_values)[o] = static_cast<uint16_t>(bits);

@@ -113,3 +113,14 @@ def test_binding_has_no_cpu_fallback():
     import torch
     with pytest.raises(ValueError):
         dstk.topk(torch.zeros(2, 16), 3)
+
+
+def test_index_type_checks():
+    P = 1 << 20  # fake 16-byte aligned device address, never dereferenced
+    base = (P, dstk.FP32, 2, 16, 16, 4, 0, 1)
+    # an index type other than int32 / int64 is rejected before anything runs
+    for bad in (-1, 2, 7):
+        assert dstk.ds_topk_ex(*base, bad, P, P, P, 0) == dstk.EINVAL
+    # int64 indices need 8-byte alignment
+    assert dstk.ds_topk_ex(*base, dstk.INDEX_INT64, P, P + 4, P, 0) == dstk.EALIGN
+    assert dstk.ds_topk_ex(0, dstk.FP32, 0, 16, 16, 4, 0, 0, dstk.INDEX_INT64, 0, 0, 0, 0) == dstk.OK
