@@ -245,3 +245,29 @@ def test_k_beyond_finite_granules(dtype):
     x = workloads.random_rows(2, 300000, dtype, 4097, style="normal")
     x[:, 2000:] = float("-inf")
     assert_parity(x, 4096, sorted_index=True, return_value=True)
+
+
+def test_concurrent_streams():
+    """Calls on different streams may overlap (the library keeps no global
+    scratch): one CTA per row, a cluster per row, one warp per row and the value
+    order, all enqueued before any synchronisation."""
+    dstk = _dstk()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cases = [
+        (workloads.random_rows(8, 4096, torch.float32, 801), 64, True),
+        (workloads.random_rows(2, 300000, torch.bfloat16, 802), 1024, True),
+        (workloads.random_rows(4 * sms + 1, 1000, torch.bfloat16, 803, style="ties"), 37, True),
+        (workloads.random_rows(16, 50000, torch.float32, 804), 512, "value"),
+    ]
+    streams = [torch.cuda.Stream() for _ in cases]
+    devs = [x.cuda() for x, _, _ in cases]
+    torch.cuda.synchronize()
+    outs = []
+    for (x, k, order), xd, s in zip(cases, devs, streams):
+        with torch.cuda.stream(s):
+            outs.append(dstk.topk(xd, k, sorted_index=order, return_value=True, stream=s))
+    torch.cuda.synchronize()
+    for (x, k, order), (gv, gi) in zip(cases, outs):
+        ov, oi, _, _ = oracle.topk(x, k, order="value" if order == "value" else "index")
+        assert torch.equal(gi.cpu(), oi)
+        assert np.array_equal(bits_of(gv.cpu()), bits_of(ov))
