@@ -53,9 +53,35 @@ SAMPLE_TOP_P = 0.9
 
 def kernel_name(w, plan) -> str:
     es = 2 if w.dtype == torch.bfloat16 else 4
+    if plan.path == 3:
+        return f"topk_unaligned_kernel<{es}>"
     if plan.path == 2:
         return f"topk_warp_rows_kernel<{es}>"
     return f"topk_rows_kernel<{es},{plan.cluster_size}>"
+
+
+def shifted(x, shift):
+    """x (contiguous) copied into a new device buffer `shift` elements past its
+    16-byte aligned start: with shift * sizeof(dtype) not a multiple of 16, no row
+    starts on a 16-byte boundary."""
+    if not shift:
+        return x
+    buf = torch.empty(x.numel() + shift + 16, dtype=x.dtype, device=x.device)
+    view = buf[shift:shift + x.numel()].view(x.shape)
+    view.copy_(x)
+    return view
+
+
+def plan_for(dstk, w, sm_count, shift):
+    """The launch plan ds_topk takes for the workload's rows at this shift (the
+    plan call assumes a 16-byte aligned x; a row stride that is not a multiple of
+    16 bytes gives the unaligned-rows plan, which depends on the batch only)."""
+    stride = w.length
+    if (shift * w.elem_size) % 16:
+        stride = w.length + 1
+        while (stride * w.elem_size) % 16 == 0:
+            stride += 1
+    return dstk.ds_topk_plan(dstk.dtype_code(w.dtype), w.batch, w.length, stride, w.k, sm_count)
 
 
 def kernel_hash() -> str:
@@ -224,7 +250,7 @@ def run_reference(args, w):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(w, None),
+        "config": _config(w, None, args.shift),
         "cpu_baseline": cb,
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "note": "reference arm = the CPU oracle (plain sort per row), host cores only",
@@ -233,8 +259,10 @@ def run_reference(args, w):
     return 0
 
 
-def _config(w, copies):
-    cfg = {"workload": f"{w.name}: {w.description}", "batch": w.batch, "len": w.length, "k": w.k,
+def _config(w, copies, shift=0):
+    cfg = {"workload": f"{w.name}: {w.description}" + (f"; rows start {shift} element(s) past a 16-byte "
+                                                        f"boundary" if shift else ""),
+           "batch": w.batch, "len": w.length, "k": w.k,
            "input_dtype": "bf16" if w.dtype == torch.bfloat16 else "fp32",
            "sorted_index": w.sorted_index, "return_value": w.return_value,
            "seed": w.seed, "parallelism": "rows independent; one GPU per rank (weak scaling)"}
@@ -254,8 +282,8 @@ def run_ours(args, w):
 
     # resident inputs: enough copies that one step's input is cold in L2
     copies = 1 if w.bytes_in >= 4 * l2 else min(64, math.ceil(4 * l2 / w.bytes_in))
-    x0 = workloads.generate(w, device=dev)
-    xs = [x0] + [x0.clone() for _ in range(copies - 1)]
+    x0 = shifted(workloads.generate(w, device=dev), args.shift)
+    xs = [x0] + [shifted(x0.contiguous(), args.shift) for _ in range(copies - 1)]
     l2_note = (f"inputs larger than L2 ({w.bytes_in / 1e6:.0f} MB per step > {l2 / 1e6:.0f} MB)"
                if copies == 1 else
                f"rotating {copies} resident input copies ({copies * w.bytes_in / 1e6:.0f} MB > 4x L2 "
@@ -264,7 +292,7 @@ def run_ours(args, w):
     idx = torch.empty((w.batch, w.k), dtype=torch.int32, device=dev)
     vals = torch.empty((w.batch, w.k), dtype=w.dtype, device=dev) if w.return_value else None
     flag = torch.zeros(1, dtype=torch.int32, device=dev)
-    rc, plan = dstk.ds_topk_plan(dt_code, w.batch, w.length, w.length, w.k, props.multi_processor_count)
+    rc, plan = plan_for(dstk, w, props.multi_processor_count, args.shift)
     assert rc == dstk.OK, dstk.status_string(rc)
 
     sampling = args.order == "sample"
@@ -339,10 +367,10 @@ def run_ours(args, w):
     per_launch_s = seconds / (args.steps * plan.launches)
     achieved = bytes_step / plan.launches / per_launch_s / 1e9
     peak, peak_src = measured_peak()
-    traffic, traffic_note = profiled_traffic(w.name)
+    traffic, traffic_note = profiled_traffic(w.name + (f"+shift{args.shift}" if args.shift else ""))
 
     # end to end through the public API with host buffers (pinned), copies inside
-    e2e = e2e_measure(w, dstk, dev, stream, min(args.steps, args.e2e_steps))
+    e2e = e2e_measure(w, dstk, dev, stream, min(args.steps, args.e2e_steps), args.shift)
     cb = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(w, min_seconds=args.cpu_seconds)
@@ -355,7 +383,7 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "u16" if w.dtype == torch.bfloat16 else "u32",
             "data": "synthetic (seeded SplitMix64 + Box-Muller, workloads.py)",
-            "config": dict(_config(w, l2_note), **({"call": f"ds_topk_sample (temperature {SAMPLE_TEMPERATURE}, "
+            "config": dict(_config(w, l2_note, args.shift), **({"call": f"ds_topk_sample (temperature {SAMPLE_TEMPERATURE}, "
                                                            f"top_p {SAMPLE_TOP_P})"} if sampling else {})),
             "rows_per_s": round(w.batch * args.steps * world / max_seconds, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
@@ -378,12 +406,12 @@ def run_ours(args, w):
     return 0
 
 
-def e2e_measure(w, dstk, dev, stream, steps):
+def e2e_measure(w, dstk, dev, stream, steps, shift=0):
     """Same metric through topk() with the input in pinned host memory: every step
     copies the batch host->device, selects, and copies the outputs back."""
     steps = max(1, steps)
     x_host = workloads.generate(w).pin_memory()
-    x_dev = torch.empty_like(x_host, device=dev)
+    x_dev = shifted(torch.empty_like(x_host, device=dev), shift)
     idx_dev = torch.empty((w.batch, w.k), dtype=torch.int32, device=dev)
     vals_dev = torch.empty((w.batch, w.k), dtype=w.dtype, device=dev) if w.return_value else None
     idx_host = torch.empty((w.batch, w.k), dtype=torch.int32).pin_memory()
@@ -422,7 +450,7 @@ def run_case(args, w):
     import sampler_topk_selection_ds_b300 as dstk
     if args.rows:
         w = w.scaled(args.rows)
-    x = workloads.generate(w, device="cuda")
+    x = shifted(workloads.generate(w, device="cuda"), args.shift)
     flag = torch.zeros(1, dtype=torch.int32, device="cuda")
     for _ in range(args.calls):
         dstk.topk(x, w.k, sorted_index=w.sorted_index, return_value=w.return_value, nan_flag=flag)
@@ -445,6 +473,9 @@ def main(argv=None):
                     help="value: value-ordered output (sorted_index 2; one more launch per call); "
                          "sample: the sampler tail ds_topk_sample (temperature 1, top_p 0.9; "
                          "three launches per call)")
+    ap.add_argument("--shift", type=int, default=0,
+                    help="place the input this many elements past a 16-byte boundary (an odd "
+                         "shift sends every row to the unaligned-rows path)")
     ap.add_argument("--case", action="store_true",
                     help="profiling case: run the workload --calls times, untimed (for ncu)")
     ap.add_argument("--rows", type=int, default=0, help="--case: use only the first ROWS rows")

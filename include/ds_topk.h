@@ -17,7 +17,8 @@
  *  - deepseek-v4-pro.uk (zh-tw), "深入 DeepSeek V4.1 全新開放推論工具包",
  *    section "DeepSelect：快速且刻意狹義的 TopK": bf16 Lightning-Indexer path and
  *    fp32 sampler path, topk <= 4096, rows need a specific alignment (callers may
- *    pad), return_value=False skips the values output, the NaN check is always on.
+ *    pad; here such rows take a slower path instead of being refused),
+ *    return_value=False skips the values output, the NaN check is always on.
  *  - github-research.aiutil.com, "deepseek-ai/DeepSelect", section 关键技术亮点:
  *    TopK does no floating-point math, so values are copied, never computed.
  *
@@ -52,7 +53,7 @@ typedef enum {
 typedef enum {
   DS_TOPK_OK = 0,       /* launched (or nothing to do: batch == 0)                      */
   DS_TOPK_EINVAL = 1,   /* bad argument; nothing was launched                            */
-  DS_TOPK_EALIGN = 2,   /* x / row stride / output pointer misaligned; nothing launched  */
+  DS_TOPK_EALIGN = 2,   /* x or an output pointer misaligned; nothing launched           */
   DS_TOPK_ECUDA = 3,    /* a CUDA runtime call failed (device query or launch)           */
   DS_TOPK_ETIMEOUT = 4  /* reserved: a bounded device-side wait expired (see flag bits)  */
 } ds_topk_status;
@@ -81,14 +82,18 @@ typedef enum {
  *                Row b starts at element b*row_stride; elements [0, len) of it
  *                are the row. Only those elements are read (padding
  *                [len, row_stride) is never read nor checked for NaN).
- *                Must be 16-byte aligned.
+ *                Must be aligned to sizeof(dtype). Rows that start on a
+ *                16-byte boundary (x 16-byte aligned and row_stride *
+ *                sizeof(dtype) a multiple of 16) take the fast paths; any other
+ *                rows take DS_TOPK_PATH_UNALIGNED, which gives the same result
+ *                more slowly (it re-reads each row once per 8-bit key digit).
  *   dtype        DS_TOPK_BF16 or DS_TOPK_FP32.
  *   batch        number of rows, >= 0. batch == 0 returns DS_TOPK_OK at once
  *                (pointers may then be NULL).
  *   len          row length, 1 <= len <= INT32_MAX.
- *   row_stride   elements between row starts, >= len;
- *                row_stride * sizeof(dtype) must be a multiple of 16 bytes
- *                (the pages' "rows need a specific alignment, callers may pad").
+ *   row_stride   elements between row starts, >= len. A multiple of 16 bytes
+ *                keeps every row on the fast paths (see x); the pages' kernel
+ *                requires that alignment and leaves the padding to callers.
  *   k            1 <= k <= min(len, DS_TOPK_MAX_K).
  *   sorted_index DS_TOPK_SORT_NONE (0), DS_TOPK_SORT_INDEX (1) or
  *                DS_TOPK_SORT_VALUE (2). 1: each output row lists its k indices
@@ -194,8 +199,11 @@ DS_TOPK_API int ds_topk_sample(const void* x, int dtype, int64_t batch, int64_t 
 typedef enum {
   DS_TOPK_PATH_ROW = 0,      /* one CTA per row                                     */
   DS_TOPK_PATH_CLUSTER = 1,  /* one thread-block cluster per row (row split in slices) */
-  DS_TOPK_PATH_WARP_ROWS = 2 /* one warp per row, several rows per CTA: many rows of at
-                                most 65536 elements with k <= 1024                   */
+  DS_TOPK_PATH_WARP_ROWS = 2, /* one warp per row, several rows per CTA: many rows of at
+                                 most 65536 elements with k <= 1024                  */
+  DS_TOPK_PATH_UNALIGNED = 3   /* one CTA per row for rows that do not start on a
+                                  16-byte boundary: exact radix selection, 8 bits of
+                                  the order key per pass over the row              */
 } ds_topk_path;
 
 /* Launch plan of one ds_topk call, as chosen by the host dispatcher. */
@@ -222,8 +230,10 @@ typedef struct {
  * ds_topk_plan — fill *plan with the launch plan ds_topk would use for these
  * sizes on a GPU with `sm_count` SMs, without touching the GPU (pure host logic;
  * runs without a device). Same validation as ds_topk for the size arguments
- * (x/output pointers are not involved). Returns DS_TOPK_OK or DS_TOPK_EINVAL /
- * DS_TOPK_EALIGN; plan must be non-NULL and sm_count >= 1.
+ * (x/output pointers are not involved: x is taken to be 16-byte aligned; an x
+ * that is not sends ds_topk to DS_TOPK_PATH_UNALIGNED whatever the plan says).
+ * Returns DS_TOPK_OK or DS_TOPK_EINVAL; plan must be non-NULL and
+ * sm_count >= 1.
  */
 DS_TOPK_API int ds_topk_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k,
                  int sm_count, ds_topk_plan_t* plan);

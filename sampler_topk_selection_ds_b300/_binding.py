@@ -26,6 +26,7 @@ MAX_K = 4096
 PATH_ROW = 0
 PATH_CLUSTER = 1
 PATH_WARP_ROWS = 2
+PATH_UNALIGNED = 3
 INDEX_INT32 = 0
 INDEX_INT64 = 1
 SORT_NONE = 0   # output order unspecified
@@ -183,8 +184,7 @@ def topk(x: torch.Tensor, k: int, sorted_index=False, return_value: bool = True,
 
 def sample(x: torch.Tensor, k: int, temperature: float, top_p: float, u: torch.Tensor,
            nan_flag: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
-    """Sampler tail on a CUDA tensor x [batch, len] (contiguous rows, 16-byte row
-    stride): TopK in value order, temperature softmax over the k survivors, top-p
+    """Sampler tail on a CUDA tensor x [batch, len] (contiguous rows): TopK in value order, temperature softmax over the k survivors, top-p
     nucleus, one draw per row with the caller's uniform numbers u (float32 CUDA
     [batch], each in [0, 1)). Returns (tokens int32 [batch], values [batch, k],
     indices int32 [batch, k])."""

@@ -19,6 +19,7 @@
 #include "warp_rows_kernel.cuh"
 #include "value_order_kernel.cuh"
 #include "sampler_kernel.cuh"
+#include "unaligned_kernel.cuh"
 
 namespace {
 
@@ -53,7 +54,9 @@ struct Plan {
   ds_topk_plan_t pub;
   Params prm;
   ds_topk_dev::WrParams wprm;
+  ds_topk_dev::UaParams uprm;
   bool warp_rows;
+  bool unaligned;
   int es;
 };
 
@@ -66,13 +69,14 @@ int validate_sizes(int dtype, int64_t batch, int64_t len, int64_t row_stride, in
   const int64_t es = dtype == DS_TOPK_BF16 ? 2 : 4;
   if (row_stride > INT64_MAX / es) return DS_TOPK_EINVAL;
   if (batch > 0 && row_stride * es > INT64_MAX / batch) return DS_TOPK_EINVAL;
-  if ((row_stride * es) % 16 != 0) return DS_TOPK_EALIGN;
   return DS_TOPK_OK;
 }
 
-// Pure host planning: how the rows map onto CTAs and clusters.
+// Pure host planning: how the rows map onto CTAs and clusters. x_aligned: x
+// starts on a 16-byte boundary (with a row stride of a multiple of 16 bytes,
+// then so does every row).
 int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, int sm_count,
-              int max_cluster, bool stage, Plan* out) {
+              int max_cluster, bool stage, bool x_aligned, Plan* out) {
   const int rc = validate_sizes(dtype, batch, len, row_stride, k);
   if (rc != DS_TOPK_OK) return rc;
   if (sm_count < 1) return DS_TOPK_EINVAL;
@@ -81,6 +85,35 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
   const int64_t nvec = ceil_div(len, vec);
   const int64_t row_bytes = len * es;
   out->warp_rows = false;
+  out->unaligned = false;
+
+  // Rows that do not all start on a 16-byte boundary: one CTA per row, radix
+  // selection over the aligned vectors that overlap the row.
+  if (!x_aligned || (row_stride * es) % 16 != 0) {
+    out->es = es;
+    out->unaligned = true;
+    ds_topk_plan_t& pl = out->pub;
+    pl.path = DS_TOPK_PATH_UNALIGNED;
+    pl.cluster_size = 1;
+    pl.threads_per_cta = ds_topk_dev::kUaThreads;
+    pl.vectors_per_granule = 1;
+    pl.grid_ctas = batch;
+    pl.granules_per_cta = 0;
+    pl.smem_bytes = 0;
+    pl.launches = batch > 0 ? 1 : 0;
+    ds_topk_dev::UaParams& u = out->uprm;
+    u.x = nullptr;
+    u.batch = batch;
+    u.row_stride_bytes = row_stride * es;
+    u.len = len;
+    u.k = k;
+    u.return_value = 0;
+    u.out_values = nullptr;
+    u.out_indices = nullptr;
+    u.idx64 = 0;
+    u.flag = nullptr;
+    return DS_TOPK_OK;
+  }
 
   // Many short rows: one warp per row (candidate indices fit 16 bits, and a
   // warp's candidate buffer of about 2k entries leaves room for 2+ CTAs per SM).
@@ -371,18 +404,30 @@ int resident_warp_rows(int smem, int sm_count) {
   return n * sm_count;
 }
 
+template <int ES>
+int resident_unaligned(int sm_count) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ds_topk_dev::topk_unaligned_kernel<ES>,
+                                                    ds_topk_dev::kUaThreads, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n * sm_count;
+}
+
 // Cached resident_clusters() per (device, dtype, cluster size, variant, shared memory);
-// the warp-rows kernel is cached as variant 2.
+// the warp-rows kernel is cached as variant 2, the unaligned-rows kernel as 3.
 int resident_cached(int dev, const Plan& pl, int sm_count) {
   const int es = pl.es, S = pl.pub.cluster_size, smem = pl.pub.smem_bytes;
-  const int gv1 = pl.warp_rows ? 2 : (pl.prm.gv == 1 ? 1 : 0);
+  const int gv1 = pl.unaligned ? 3 : pl.warp_rows ? 2 : (pl.prm.gv == 1 ? 1 : 0);
   std::lock_guard<std::mutex> lock(g_mu);
   for (int i = 0; i < g_residency_used; ++i) {
     const ResidencyEntry& e = g_residency[i];
     if (e.dev == dev && e.es == es && e.S == S && e.gv1 == gv1 && e.smem == smem) return e.clusters;
   }
   int n;
-  if (gv1 == 2) n = es == 2 ? resident_warp_rows<2>(smem, sm_count) : resident_warp_rows<4>(smem, sm_count);
+  if (gv1 == 3) n = es == 2 ? resident_unaligned<2>(sm_count) : resident_unaligned<4>(sm_count);
+  else if (gv1 == 2) n = es == 2 ? resident_warp_rows<2>(smem, sm_count) : resident_warp_rows<4>(smem, sm_count);
   else if (es == 2) n = gv1 ? resident_variant<2, true>(S, smem, sm_count) : resident_variant<2, false>(S, smem, sm_count);
   else n = gv1 ? resident_variant<4, true>(S, smem, sm_count) : resident_variant<4, false>(S, smem, sm_count);
   if (g_residency_used < kResidencySlots) g_residency[g_residency_used++] = {dev, es, S, gv1, smem, n};
@@ -443,7 +488,19 @@ cudaError_t launch_warp_rows(const Plan& pl, cudaStream_t stream) {
 }
 
 template <int ES>
+cudaError_t launch_unaligned(const Plan& pl, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.pub.grid_ctas), 1, 1);
+  cfg.blockDim = dim3(ds_topk_dev::kUaThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, ds_topk_dev::topk_unaligned_kernel<ES>, pl.uprm);
+}
+
+template <int ES>
 cudaError_t launch_dtype(const Plan& pl, cudaStream_t stream) {
+  if (pl.unaligned) return launch_unaligned<ES>(pl, stream);
   if (pl.warp_rows) return launch_warp_rows<ES>(pl, stream);
   return pl.prm.gv == 1 ? launch_variant<ES, true>(pl, stream) : launch_variant<ES, false>(pl, stream);
 }
@@ -519,9 +576,10 @@ extern "C" int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, 
   if (!x || !out_indices || !nan_flag || (return_value && !out_values)) return DS_TOPK_EINVAL;
   const int es = dtype == DS_TOPK_BF16 ? 2 : 4;
   const int idx64 = index_type == DS_TOPK_INDEX_INT64 ? 1 : 0;
-  if (misaligned(x, 16) || misaligned(out_indices, idx64 ? 8 : 4) || misaligned(nan_flag, 4) ||
+  if (misaligned(x, es) || misaligned(out_indices, idx64 ? 8 : 4) || misaligned(nan_flag, 4) ||
       (return_value && misaligned(out_values, es)))
     return DS_TOPK_EALIGN;
+  const bool x_aligned = !misaligned(x, 16);
 
   DeviceInfo dev;
   rc = device_info(&dev);
@@ -531,8 +589,27 @@ extern "C" int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, 
   cudaGetDevice(&dev_id);
   // With the next-row prefetch, if more rows than co-resident clusters (so that a
   // persistent cluster walks several rows); otherwise without it.
-  rc = make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, false, &pl);
+  rc = make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, false, x_aligned, &pl);
   if (rc != DS_TOPK_OK) return rc;
+  if (pl.unaligned) {
+    pl.uprm.x = static_cast<const char*>(x);
+    pl.uprm.return_value = return_value;
+    pl.uprm.out_values = return_value ? out_values : nullptr;
+    pl.uprm.out_indices = out_indices;
+    pl.uprm.idx64 = idx64;
+    pl.uprm.flag = nan_flag;
+    // every resident CTA walks rows with a stride of the grid
+    const int resident_ctas = resident_cached(dev_id, pl, dev.sm_count);
+    if (resident_ctas > 0 && pl.pub.grid_ctas > resident_ctas) pl.pub.grid_ctas = resident_ctas;
+    if (pl.pub.grid_ctas > INT32_MAX) pl.pub.grid_ctas = INT32_MAX;
+    const cudaError_t e = es == 2 ? launch_dtype<2>(pl, stream) : launch_dtype<4>(pl, stream);
+    if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) {
+      cudaGetLastError();
+      return DS_TOPK_ECUDA;
+    }
+    return finish_order(es, sorted_index, x, batch, len, row_stride, k, return_value, out_values, out_indices,
+                        idx64, dev.sm_count, stream);
+  }
   if (pl.warp_rows) {
     pl.wprm.x = static_cast<const char*>(x);
     pl.wprm.return_value = return_value;
@@ -553,7 +630,7 @@ extern "C" int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, 
   int resident = resident_cached(dev_id, pl, dev.sm_count);
   if (resident > 0 && batch > resident) {
     Plan ps;
-    if (make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, true, &ps) ==
+    if (make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, true, true, &ps) ==
             DS_TOPK_OK &&
         ps.prm.stage_vecs > 0) {
       const int rs = resident_cached(dev_id, ps, dev.sm_count);
@@ -641,7 +718,7 @@ extern "C" int ds_topk_plan(int dtype, int64_t batch, int64_t len, int64_t row_s
                             int sm_count, ds_topk_plan_t* plan) {
   if (!plan) return DS_TOPK_EINVAL;
   Plan pl;
-  const int rc = make_plan(dtype, batch, len, row_stride, k, sm_count, kMaxCluster, false, &pl);
+  const int rc = make_plan(dtype, batch, len, row_stride, k, sm_count, kMaxCluster, false, true, &pl);
   if (rc == DS_TOPK_OK) *plan = pl.pub;
   return rc;
 }
@@ -650,7 +727,7 @@ extern "C" const char* ds_topk_status_string(int status) {
   switch (status) {
     case DS_TOPK_OK: return "ok";
     case DS_TOPK_EINVAL: return "invalid argument";
-    case DS_TOPK_EALIGN: return "misaligned pointer or row stride";
+    case DS_TOPK_EALIGN: return "misaligned pointer";
     case DS_TOPK_ECUDA: return "CUDA runtime error";
     case DS_TOPK_ETIMEOUT: return "device-side wait timed out";
     default: return "unknown status";

@@ -58,9 +58,8 @@ P = 1 << 20  # a 16-byte-aligned fake address
     ((P, 0, 1, 16, 16, 1, 0, 1, P, 0, P), dstk.EINVAL),          # out_indices NULL
     ((P, 0, 1, 16, 16, 1, 0, 1, P, P, 0), dstk.EINVAL),          # nan_flag NULL
     ((P, 0, 1, 16, 16, 1, 0, 1, 0, P, P), dstk.EINVAL),          # values requested, NULL
-    ((P + 8, 0, 1, 16, 16, 1, 0, 1, P, P, P), dstk.EALIGN),      # x not 16-byte aligned
-    ((P, 0, 2, 12, 12, 1, 0, 1, P, P, P), dstk.EALIGN),          # bf16 stride 24 bytes
-    ((P, 1, 2, 6, 6, 1, 0, 1, P, P, P), dstk.EALIGN),            # fp32 stride 24 bytes
+    ((P + 1, 0, 1, 16, 16, 1, 0, 1, P, P, P), dstk.EALIGN),      # bf16 x not 2-byte aligned
+    ((P + 2, 1, 1, 16, 16, 1, 0, 1, P, P, P), dstk.EALIGN),      # fp32 x not 4-byte aligned
     ((P, 0, 1, 16, 16, 1, 0, 1, P, P + 2, P), dstk.EALIGN),      # out_indices misaligned
     ((P, 0, 1, 16, 16, 1, 0, 1, P, P, P + 1), dstk.EALIGN),      # flag misaligned
     ((P, 1, 1, 16, 16, 1, 0, 1, P + 2, P, P), dstk.EALIGN),      # fp32 values misaligned
@@ -106,7 +105,22 @@ def test_plan_shapes():
     # validation is shared with ds_topk
     assert dstk.ds_topk_plan(dstk.FP32, 1, 10, 10, 11, 148)[0] == dstk.EINVAL
     assert dstk.ds_topk_plan(dstk.FP32, 1, 10, 12, 5, 0)[0] == dstk.EINVAL
-    assert dstk.ds_topk_plan(dstk.BF16, 2, 10, 10, 5, 148)[0] == dstk.EALIGN
+
+def test_plan_unaligned_rows():
+    """Row strides that are not a multiple of 16 bytes put some rows off a
+    16-byte boundary: one CTA per row on the unaligned-rows path, whatever the
+    sizes (a stride of a multiple of 16 bytes keeps the other paths)."""
+    for dtype, stride in ((dstk.BF16, 10), (dstk.BF16, 32769), (dstk.FP32, 6), (dstk.FP32, 129281)):
+        for batch, k in ((2, 5), (16384, 512), (64, 4)):
+            length = stride if stride > 10 else stride - 1
+            rc, p = dstk.ds_topk_plan(dtype, batch, length, stride, min(k, length), 148)
+            assert rc == 0 and p.path == dstk.PATH_UNALIGNED, (dtype, stride, batch)
+            assert p.cluster_size == 1 and p.grid_ctas == batch and p.smem_bytes == 0
+            assert p.threads_per_cta == 512 and p.launches == 1
+    rc, p = dstk.ds_topk_plan(dstk.BF16, 2, 10, 16, 5, 148)  # 32-byte stride: fast path
+    assert rc == 0 and p.path == dstk.PATH_ROW
+    rc, p = dstk.ds_topk_plan(dstk.FP32, 0, 10, 10, 5, 148)
+    assert rc == 0 and p.path == dstk.PATH_UNALIGNED and p.launches == 0
 
 
 def test_binding_has_no_cpu_fallback():

@@ -41,13 +41,15 @@ def _near_boundary(v, temperature, top_p, u, gpu_pos):
     return False
 
 
-def check_sample(x, k, temperature, top_p, seed):
+def check_sample(x, k, temperature, top_p, seed, xd=None):
+    """x: the rows on the CPU (the oracle's input); xd: the same rows on the
+    device if they are to be read from a particular layout (default x.cuda())."""
     import sampler_topk_selection_ds_b300 as dstk
     b = x.shape[0]
     u = np.random.default_rng(seed).random(b).astype(np.float32)
     ut = torch.from_numpy(u).cuda()
     flag = torch.zeros(1, dtype=torch.int32, device="cuda")
-    tok, gv, gi = dstk.sample(x.cuda(), k, temperature, top_p, ut, nan_flag=flag)
+    tok, gv, gi = dstk.sample(x.cuda() if xd is None else xd, k, temperature, top_p, ut, nan_flag=flag)
     torch.cuda.synchronize()
     tok, gv, gi = tok.cpu().numpy(), gv.cpu(), gi.cpu()
     otok, opos, oidx, ovals, row_nan = osam.sample(x, k, temperature, top_p, u.astype(np.float64))
