@@ -97,9 +97,13 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
     pl.cluster_size = 1;
     pl.threads_per_cta = ds_topk_dev::kUaThreads;
     pl.vectors_per_granule = 1;
+    // candidate keys of a guessed threshold (about 1.5 k expected; also holds
+    // the first-row sample)
+    int64_t cap = 4 * static_cast<int64_t>(k) + 2048;
+    if (cap < ds_topk_dev::kUaSampleKeys) cap = ds_topk_dev::kUaSampleKeys;
     pl.grid_ctas = batch;
-    pl.granules_per_cta = 0;
-    pl.smem_bytes = 0;
+    pl.granules_per_cta = cap;
+    pl.smem_bytes = static_cast<int32_t>(cap * 4);
     pl.launches = batch > 0 ? 1 : 0;
     ds_topk_dev::UaParams& u = out->uprm;
     u.x = nullptr;
@@ -107,6 +111,7 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
     u.row_stride_bytes = row_stride * es;
     u.len = len;
     u.k = k;
+    u.cap = static_cast<int32_t>(cap);
     u.return_value = 0;
     u.out_values = nullptr;
     u.out_indices = nullptr;
@@ -299,6 +304,11 @@ cudaError_t prepare_dtype() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(ds_topk_dev::topk_warp_rows_kernel<ES>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+  // the unaligned-rows kernel's largest candidate buffer (k = DS_TOPK_MAX_K); it
+  // also has static shared memory, so the full per-CTA limit would be refused
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ds_topk_dev::topk_unaligned_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (4 * DS_TOPK_MAX_K + 2048) * 4);
   return e;
 }
 
@@ -405,10 +415,10 @@ int resident_warp_rows(int smem, int sm_count) {
 }
 
 template <int ES>
-int resident_unaligned(int sm_count) {
+int resident_unaligned(int smem, int sm_count) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ds_topk_dev::topk_unaligned_kernel<ES>,
-                                                    ds_topk_dev::kUaThreads, 0) != cudaSuccess) {
+                                                    ds_topk_dev::kUaThreads, smem) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -426,7 +436,7 @@ int resident_cached(int dev, const Plan& pl, int sm_count) {
     if (e.dev == dev && e.es == es && e.S == S && e.gv1 == gv1 && e.smem == smem) return e.clusters;
   }
   int n;
-  if (gv1 == 3) n = es == 2 ? resident_unaligned<2>(sm_count) : resident_unaligned<4>(sm_count);
+  if (gv1 == 3) n = es == 2 ? resident_unaligned<2>(smem, sm_count) : resident_unaligned<4>(smem, sm_count);
   else if (gv1 == 2) n = es == 2 ? resident_warp_rows<2>(smem, sm_count) : resident_warp_rows<4>(smem, sm_count);
   else if (es == 2) n = gv1 ? resident_variant<2, true>(S, smem, sm_count) : resident_variant<2, false>(S, smem, sm_count);
   else n = gv1 ? resident_variant<4, true>(S, smem, sm_count) : resident_variant<4, false>(S, smem, sm_count);
@@ -492,7 +502,7 @@ cudaError_t launch_unaligned(const Plan& pl, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pl.pub.grid_ctas), 1, 1);
   cfg.blockDim = dim3(ds_topk_dev::kUaThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = static_cast<size_t>(pl.pub.smem_bytes);
   cfg.stream = stream;
   cfg.numAttrs = 0;
   return cudaLaunchKernelEx(&cfg, ds_topk_dev::topk_unaligned_kernel<ES>, pl.uprm);

@@ -115,7 +115,9 @@ def test_plan_unaligned_rows():
             length = stride if stride > 10 else stride - 1
             rc, p = dstk.ds_topk_plan(dtype, batch, length, stride, min(k, length), 148)
             assert rc == 0 and p.path == dstk.PATH_UNALIGNED, (dtype, stride, batch)
-            assert p.cluster_size == 1 and p.grid_ctas == batch and p.smem_bytes == 0
+            kk = min(k, length)
+            assert p.cluster_size == 1 and p.grid_ctas == batch
+            assert p.granules_per_cta == max(4 * kk + 2048, 8192) and p.smem_bytes == 4 * p.granules_per_cta
             assert p.threads_per_cta == 512 and p.launches == 1
     rc, p = dstk.ds_topk_plan(dstk.BF16, 2, 10, 16, 5, 148)  # 32-byte stride: fast path
     assert rc == 0 and p.path == dstk.PATH_ROW

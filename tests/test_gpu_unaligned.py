@@ -110,6 +110,23 @@ def test_unaligned_many_rows(dtype):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_unaligned_guess_takes_a_bin_whole(dtype):
+    """Rows with exactly k elements at 5.0, ten at 4.5 and the rest below 3: from
+    the second row on, a CTA guesses the threshold from the previous row, the
+    candidates are the k fives, and the radix over them takes a whole 8-bit bin
+    whose lower end lies below the guess (the 4.5s share that bin and must not be
+    selected)."""
+    k = 96
+    x = workloads.random_rows(600, 6000, dtype, 48, style="normal").clamp(max=2.9)
+    for b in range(x.shape[0]):
+        cols = torch.randperm(6000, generator=torch.Generator().manual_seed(b))
+        x[b, cols[:k]] = 5.0
+        x[b, cols[k:k + 10]] = 4.5
+    check(x, k, 1, 6001, sorted_index=True)
+    check(x, k + 5, 1, 6001)  # five of the 4.5s by lowest index
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_unaligned_nan_flag(dtype):
     x = workloads.random_rows(6, 5001, dtype, 43, style="normal")
     x[0, 0] = float("nan")
