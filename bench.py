@@ -20,7 +20,6 @@ from __future__ import annotations
 import argparse
 import csv
 import dataclasses
-import glob
 import hashlib
 import io
 import json
@@ -43,8 +42,16 @@ METRIC = "effective HBM GB/s and rows/s for batched TopK (bf16 indexer, fp32 sam
 DEFAULT_WORKLOAD = "c2"
 L2_BYTES_FALLBACK = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6400.0
-KERNEL_SOURCES = sorted(os.path.relpath(f, ROOT) for f in
-                        glob.glob(os.path.join(ROOT, "sampler_topk_selection_ds_b300", "csrc", "*.cu*")))
+CSRC = os.path.join("sampler_topk_selection_ds_b300", "csrc")
+# The sources each selection kernel is built from: its own header, the shared
+# device helpers, the host file that plans and launches it, and the C header.
+_COMMON_SOURCES = [os.path.join(CSRC, "topk_kernel.cuh"), os.path.join(CSRC, "ds_topk.cu"),
+                   os.path.join("include", "ds_topk.h")]
+KERNEL_SOURCES = {
+    "topk_rows_kernel": _COMMON_SOURCES,
+    "topk_warp_rows_kernel": _COMMON_SOURCES + [os.path.join(CSRC, "warp_rows_kernel.cuh")],
+    "topk_unaligned_kernel": _COMMON_SOURCES + [os.path.join(CSRC, "unaligned_kernel.cuh")],
+}
 
 
 SAMPLE_TEMPERATURE = 1.0
@@ -84,9 +91,10 @@ def plan_for(dstk, w, sm_count, shift):
     return dstk.ds_topk_plan(dstk.dtype_code(w.dtype), w.batch, w.length, stride, w.k, sm_count)
 
 
-def kernel_hash() -> str:
+def kernel_hash(kernel: str) -> str:
+    """Hash of the sources the named kernel (e.g. "topk_warp_rows_kernel<2>") is built from."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel.split("<")[0]]:
         with open(os.path.join(ROOT, rel), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -102,7 +110,7 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of the dominant kernel, from the committed ncu summary
     of this workload (a line `bench-traffic: workload=.. kernel_hash=..
     dram_bytes_per_launch=..` in profiles/*.md), if it was taken on the current
@@ -125,7 +133,7 @@ def profiled_traffic(workload: str):
     if found is None:
         return None, None
     kv, fn = found
-    if kv.get("kernel_hash") != kernel_hash():
+    if kv.get("kernel_hash") != kernel_hash(kernel):
         return None, f"stale: {fn} was captured on kernel {kv.get('kernel_hash')}"
     return int(kv["dram_bytes_per_launch"]), f"ncu capture summarised in profiles/{fn}"
 
@@ -367,7 +375,8 @@ def run_ours(args, w):
     per_launch_s = seconds / (args.steps * plan.launches)
     achieved = bytes_step / plan.launches / per_launch_s / 1e9
     peak, peak_src = measured_peak()
-    traffic, traffic_note = profiled_traffic(w.name + (f"+shift{args.shift}" if args.shift else ""))
+    traffic, traffic_note = profiled_traffic(w.name + (f"+shift{args.shift}" if args.shift else ""),
+                                             kernel_name(w, plan))
 
     # end to end through the public API with host buffers (pinned), copies inside
     e2e = e2e_measure(w, dstk, dev, stream, min(args.steps, args.e2e_steps), args.shift)
@@ -391,7 +400,7 @@ def run_ours(args, w):
                          "peak_source": peak_src + (" (of measured)" if peak_src != "fallback" else " (of fallback)"),
                          "traffic": traffic, "traffic_note": traffic_note,
                          "kernel": kernel_name(w, plan),
-                         "kernel_hash": kernel_hash()},
+                         "kernel_hash": kernel_hash(kernel_name(w, plan))},
             "e2e": e2e,
             "gpu_launches": args.steps * launches,
             "plan": plan.as_dict(),
