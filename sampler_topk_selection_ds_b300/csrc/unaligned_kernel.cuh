@@ -241,6 +241,10 @@ __global__ void __launch_bounds__(kUaThreads, 2) topk_unaligned_kernel(const UaP
     bool exact = false;
     if (guess) {
       bool nan_seen = false;
+      // the threshold as a value, for packed compares that mark a superset of the
+      // elements with key >= t (every NaN included); each is then checked by key
+      const float tval = key_threshold_value<ES>(t);
+      const uint32_t tv2 = (__float_as_uint(tval) >> 16) * 0x00010001u;
       for (int64_t qb = 0; qb < nq; qb += static_cast<int64_t>(kUaThreads) * kUaUnroll) {
         uint4 w[kUaUnroll];
         uint32_t val[kUaUnroll];
@@ -254,24 +258,16 @@ __global__ void __launch_bounds__(kUaThreads, 2) topk_unaligned_kernel(const UaP
 #pragma unroll
         for (int u = 0; u < kUaUnroll; ++u) {
           if (val[u] == 0u || (val[u] == kFull && ua_vmax_key<ES>(w[u]) < t)) continue;
-          uint32_t keys[VEC];
-          uint32_t c = 0u;
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) {
+          uint32_t m = cand_mask<ES>(w[u], tval, tv2) & val[u];
+          while (m) {
+            const int e = __ffs(m) - 1;
+            m &= m - 1u;
             const uint32_t bits = elem_bits<ES>(w[u], e);
-            const bool in = (val[u] >> e) & 1u;
-            nan_seen |= in && is_nan_bits<ES>(bits);
-            keys[e] = key_of<ES>(bits);
-            c += (in && keys[e] >= t) ? 1u : 0u;
-          }
-          if (c) {
-            uint32_t pos = atomicAdd(&sh.count, c);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              if (((val[u] >> e) & 1u) && keys[e] >= t) {
-                if (pos < cap) cand[pos] = keys[e];
-                ++pos;
-              }
+            nan_seen |= is_nan_bits<ES>(bits);
+            const uint32_t key = key_of<ES>(bits);
+            if (key >= t) {
+              const uint32_t pos = atomicAdd(&sh.count, 1u);
+              if (pos < cap) cand[pos] = key;
             }
           }
         }
@@ -342,6 +338,8 @@ __global__ void __launch_bounds__(kUaThreads, 2) topk_unaligned_kernel(const UaP
     uint32_t base_gt = 0u, base_eq = 0u;
     const int64_t row_out = row * static_cast<int64_t>(k);
     VT* ov = p.return_value ? static_cast<VT*>(p.out_values) + row_out : nullptr;
+    const float Tval = key_threshold_value<ES>(T);
+    const uint32_t Tv2 = (__float_as_uint(Tval) >> 16) * 0x00010001u;
     int par = 0;
     for (int64_t tb = 0; tb < nq; tb += static_cast<int64_t>(kUaThreads) * kUaOutVecs, par ^= 1) {
       const int64_t q0 = tb + static_cast<int64_t>(tid) * kUaOutVecs;
@@ -354,15 +352,17 @@ __global__ void __launch_bounds__(kUaThreads, 2) topk_unaligned_kernel(const UaP
         if (q0 + u < nq) {
           w[u] = ua_load<ES>(abase, q0 + u, lead, p.len, val[u]);
           if (val[u] == kFull && ua_vmax_key<ES>(w[u]) < T) val[u] = 0u;  // nothing selected here
+          // from here on val[u] marks a superset of the lanes with key >= T
+          if (val[u] != 0u) val[u] &= cand_mask<ES>(w[u], Tval, Tv2);
         }
       }
       uint32_t cg = 0u, ce = 0u;
 #pragma unroll
       for (int u = 0; u < kUaOutVecs; ++u) {
-        if (val[u] == 0u) continue;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          if (!((val[u] >> e) & 1u)) continue;
+        uint32_t m = val[u];
+        while (m) {
+          const int e = __ffs(m) - 1;
+          m &= m - 1u;
           const uint32_t key = key_of<ES>(elem_bits<ES>(w[u], e));
           cg += key > T;
           ce += key == T;
@@ -390,10 +390,10 @@ __global__ void __launch_bounds__(kUaThreads, 2) topk_unaligned_kernel(const UaP
       if (v != 0u) {
 #pragma unroll
         for (int u = 0; u < kUaOutVecs; ++u) {
-          if (val[u] == 0u) continue;
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            if (!((val[u] >> e) & 1u)) continue;
+          uint32_t m = val[u];
+          while (m) {
+            const int e = __ffs(m) - 1;
+            m &= m - 1u;
             const uint32_t bits = elem_bits<ES>(w[u], e);
             const uint32_t key = key_of<ES>(bits);
             const int64_t col = (q0 + u) * VEC + e - lead;
