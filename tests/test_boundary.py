@@ -140,3 +140,31 @@ def test_index_type_checks():
     # int64 indices need 8-byte alignment
     assert dstk.ds_topk_ex(*base, dstk.INDEX_INT64, P, P + 4, P, 0) == dstk.EALIGN
     assert dstk.ds_topk_ex(0, dstk.FP32, 0, 16, 16, 4, 0, 0, dstk.INDEX_INT64, 0, 0, 0, 0) == dstk.OK
+
+
+def test_bench_shift_layout_and_plan():
+    """bench.py --shift: the copy sits `shift` elements past an aligned start with
+    the same contents, and the plan it reports is the unaligned-rows plan exactly
+    when the shift breaks 16-byte alignment."""
+    import torch
+
+    import bench
+    import workloads
+    x = torch.arange(24, dtype=torch.float32).view(4, 6)
+    for shift in (0, 1, 3):
+        y = bench.shifted(x, shift)
+        assert torch.equal(y, x) and y.stride() == x.stride()
+        if shift == 0:
+            assert y.data_ptr() == x.data_ptr()  # no copy
+        else:
+            assert y.data_ptr() % 16 == shift * 4 % 16  # the buffer's start is 16-byte aligned
+    c4 = workloads.WORKLOADS["c4"]  # bf16 rows of 65536 bytes
+    for shift, path in ((0, dstk.PATH_WARP_ROWS), (1, dstk.PATH_UNALIGNED), (7, dstk.PATH_UNALIGNED),
+                        (8, dstk.PATH_WARP_ROWS)):
+        rc, p = bench.plan_for(dstk, c4, 148, shift)
+        assert rc == dstk.OK and p.path == path, (shift, p.path)
+        assert bench.kernel_name(c4, p).startswith("topk_unaligned" if path == dstk.PATH_UNALIGNED
+                                                   else "topk_warp_rows")
+    c2 = workloads.WORKLOADS["c2"]  # fp32: a 4-element shift keeps 16-byte alignment
+    assert bench.plan_for(dstk, c2, 148, 4)[1].path == dstk.PATH_CLUSTER
+    assert bench.plan_for(dstk, c2, 148, 2)[1].path == dstk.PATH_UNALIGNED
