@@ -141,7 +141,10 @@ def topk(x: torch.Tensor, k: int, sorted_index=False, return_value: bool = True,
          out: Optional[Tuple[Optional[torch.Tensor], torch.Tensor]] = None,
          stream: Optional[torch.cuda.Stream] = None, index_dtype: torch.dtype = torch.int32):
     """TopK of each row of a CUDA tensor x [batch, row_stride] (row stride may
-    exceed `length`, the number of valid columns; padding is never read).
+    exceed `length`, the number of valid columns; padding is never read). Rows
+    need not start on 16-byte boundaries: such rows (an offset view, or a row
+    stride that is not a multiple of 16 bytes) take the slower unaligned-rows
+    kernel with the same result.
 
     sorted_index: False/True (unspecified / ascending index), or "value"
     (SORT_VALUE: value descending, equal values by ascending index).
