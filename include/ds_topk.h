@@ -212,15 +212,16 @@ typedef struct {
   int32_t cluster_size;        /* CTAs cooperating on one row (1 for DS_TOPK_PATH_ROW) */
   int32_t threads_per_cta;
   int32_t vectors_per_granule; /* 16-byte vectors summarised by one granule maximum
-                                  (1 on DS_TOPK_PATH_WARP_ROWS: vectors are tested one
-                                  by one)                                              */
+                                  (1 on DS_TOPK_PATH_WARP_ROWS and
+                                  DS_TOPK_PATH_UNALIGNED: vectors are tested one by one) */
   int64_t grid_ctas;           /* CTAs if every row had its own cluster (warp rows: if
                                   every 8 rows had their own CTA); ds_topk launches at
                                   most as many as can be co-resident, and each
                                   persistent cluster (warp) then walks rows with a
                                   stride                                               */
   int64_t granules_per_cta;    /* size of the per-CTA granule-maximum array; on
-                                  DS_TOPK_PATH_WARP_ROWS the candidate slots per warp  */
+                                  DS_TOPK_PATH_WARP_ROWS the candidate slots per warp,
+                                  on DS_TOPK_PATH_UNALIGNED the candidate slots per CTA */
   int32_t smem_bytes;          /* dynamic shared memory per CTA                        */
   int32_t launches;            /* kernel launches per call with sorted_index 0 or 1
                                   (DS_TOPK_SORT_VALUE adds one)                        */
