@@ -91,12 +91,40 @@ def plan_for(dstk, w, sm_count, shift):
     return dstk.ds_topk_plan(dstk.dtype_code(w.dtype), w.batch, w.length, stride, w.k, sm_count)
 
 
+def code_only(src: str) -> str:
+    """C/C++/CUDA source without its comments and with whitespace runs collapsed,
+    so that edits to comments or layout leave a kernel's hash unchanged. String
+    and character literals are kept as written."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            out.append(" ")
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_hash(kernel: str) -> str:
-    """Hash of the sources the named kernel (e.g. "topk_warp_rows_kernel<2>") is built from."""
+    """Hash of the code (comments aside) of the sources the named kernel (e.g.
+    "topk_warp_rows_kernel<2>") is built from."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel.split("<")[0]]:
-        with open(os.path.join(ROOT, rel), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

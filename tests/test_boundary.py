@@ -168,3 +168,17 @@ def test_bench_shift_layout_and_plan():
     c2 = workloads.WORKLOADS["c2"]  # fp32: a 4-element shift keeps 16-byte alignment
     assert bench.plan_for(dstk, c2, 148, 4)[1].path == dstk.PATH_CLUSTER
     assert bench.plan_for(dstk, c2, 148, 2)[1].path == dstk.PATH_UNALIGNED
+
+
+def test_bench_kernel_hash_ignores_comments_only():
+    """The hash that ties a profile's DRAM traffic to a kernel covers code, not
+    comments or layout: a comment edit keeps it, a code edit changes it."""
+    import bench
+    base = 'int f(int a) { return a + 1; } // one\nconst char* s = "a // b";\n'
+    assert bench.code_only(base) == bench.code_only(
+        '/* a note */ int f(int a)  {\n  return a + 1;  // two\n}\nconst char* s = "a // b";')
+    assert bench.code_only(base) != bench.code_only(base.replace("a + 1", "a + 2"))
+    assert bench.code_only(base) != bench.code_only(base.replace('"a // b"', '"a // c"'))
+    hashes = {bench.kernel_hash(k) for k in ("topk_rows_kernel<4,4>", "topk_warp_rows_kernel<2>",
+                                             "topk_unaligned_kernel<2>")}
+    assert len(hashes) == 3
