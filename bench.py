@@ -1,15 +1,22 @@
 """Benchmark of batched row-wise TopK on B300: effective HBM GB/s and rows/s.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c4] [--impl ours|reference]
 
 A step is one ds_topk call over one batch of the workload (the whole hot path:
 load, NaN check, threshold, radix select, ordered output write). The timed
-region holds exactly K steps replayed from CUDA graphs, bracketed by a barrier
-and a device synchronize; each step reads a different resident copy of the
-input whenever one batch fits in L2, so every step streams its input from HBM.
-Rank 0 prints one JSON line. Under torchrun every rank runs the same workload
-on its own GPU (rows are independent: no collective on the data path), and the
-value is the bytes of all ranks over the slowest rank's time.
+region holds exactly K steps replayed from CUDA graphs that were each replayed
+once before it, bracketed by a barrier and a device synchronize. Every step
+reads its input from HBM: the decode-shaped indexer batch (1.07 GB) is larger
+than L2, and smaller workloads rotate over resident copies that together exceed
+four times L2. Rank 0 prints one JSON line. Under torchrun every rank runs the
+same workload on its own GPU (rows are independent: no collective on the data
+path), and the value is the bytes of all ranks over the slowest rank's time.
+
+The line's headline is the decode-shaped bf16 indexer call (16384 rows of 32768,
+k=512), the largest single-GPU workload. The other workloads (fp32 sampler,
+bf16 indexer prefill, adversarial rows, the small fp32 case) ride along in the
+same line under "per_workload", each timed over at least --min-ms of device
+work, with its own roofline fraction and CPU-oracle baseline.
 
 The metric is the pages' own: effective memory bandwidth, (input bytes read +
 output bytes written) / time, because TopK does no floating-point math
@@ -39,9 +46,11 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 METRIC = "effective HBM GB/s and rows/s for batched TopK (bf16 indexer, fp32 sampler)"
-DEFAULT_WORKLOAD = "c2"
+DEFAULT_WORKLOAD = "c4"
+EXTRA_WORKLOADS = ("c2", "c5", "c3", "c1")
 L2_BYTES_FALLBACK = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6400.0
+TRAFFIC_FILE = os.path.join("profiles", "traffic.json")
 CSRC = os.path.join("sampler_topk_selection_ds_b300", "csrc")
 # The sources each selection kernel is built from: its own header, the shared
 # device helpers, the host file that plans and launches it, and the C header.
@@ -52,7 +61,6 @@ KERNEL_SOURCES = {
     "topk_warp_rows_kernel": _COMMON_SOURCES + [os.path.join(CSRC, "warp_rows_kernel.cuh")],
     "topk_unaligned_kernel": _COMMON_SOURCES + [os.path.join(CSRC, "unaligned_kernel.cuh")],
 }
-
 
 SAMPLE_TEMPERATURE = 1.0
 SAMPLE_TOP_P = 0.9
@@ -139,31 +147,24 @@ def measured_peak():
 
 
 def profiled_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch of the dominant kernel, from the committed ncu summary
-    of this workload (a line `bench-traffic: workload=.. kernel_hash=..
-    dram_bytes_per_launch=..` in profiles/*.md), if it was taken on the current
-    kernel source; else None."""
-    pdir = os.path.join(ROOT, "profiles")
-    found = None
+    """DRAM bytes (read + write) per launch of the dominant kernel on this
+    workload, from the ncu figures recorded in the traffic data file
+    (profiles/traffic.json: workload -> kernel, kernel_hash,
+    dram_bytes_per_launch, summary), if they were taken on the current kernel
+    code; else None with the reason."""
     try:
-        names = sorted(os.listdir(pdir))
-    except OSError:
-        return None, None
-    for fn in names:
-        if not fn.endswith(".md"):
-            continue
-        with open(os.path.join(pdir, fn), encoding="utf-8") as fh:
-            for line in fh:
-                if line.startswith("bench-traffic:"):
-                    kv = dict(t.split("=", 1) for t in line.split()[1:] if "=" in t)
-                    if kv.get("workload") == workload:
-                        found = (kv, fn)
-    if found is None:
-        return None, None
-    kv, fn = found
-    if kv.get("kernel_hash") != kernel_hash(kernel):
-        return None, f"stale: {fn} was captured on kernel {kv.get('kernel_hash')}"
-    return int(kv["dram_bytes_per_launch"]), f"ncu capture summarised in profiles/{fn}"
+        with open(os.path.join(ROOT, TRAFFIC_FILE), encoding="utf-8") as fh:
+            table = json.load(fh)
+    except (OSError, ValueError):
+        return None, "no traffic data file"
+    entry = table.get(workload)
+    if not entry:
+        return None, f"no ncu traffic recorded for {workload}"
+    if entry.get("kernel") != kernel:
+        return None, f"recorded traffic is for {entry.get('kernel')}, not {kernel}"
+    if entry.get("kernel_hash") != kernel_hash(kernel):
+        return None, f"stale: recorded on kernel code {entry.get('kernel_hash')}"
+    return int(entry["dram_bytes_per_launch"]), f"ncu capture summarised in {entry.get('summary')}"
 
 
 class ClockSampler:
@@ -176,6 +177,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.out = ""
 
     def __enter__(self):
         try:
@@ -200,7 +202,7 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
         return False
 
-    def summary(self, t_start: float, t_end: float):
+    def summary(self):
         rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
@@ -218,7 +220,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
-def _dist_setup(n_gpus: int):
+def _dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -254,160 +256,275 @@ def aggregate_value(bytes_per_step: int, steps: int, world: int, max_seconds: fl
     return bytes_per_step * steps * world / max_seconds / 1e9
 
 
-def cpu_baseline(w: workloads.Workload, min_seconds: float):
+def sample_rows(w: workloads.Workload, max_rows: int):
+    """A bounded, evenly spread sample of the workload's rows (all of them if few)."""
+    if w.batch <= max_rows:
+        return list(range(w.batch))
+    step = w.batch / max_rows
+    return [int(i * step) for i in range(max_rows)]
+
+
+def _oracle_gbs(w, x, nthreads, min_seconds, repeats):
+    """`repeats` timings of the oracle on the sample x, each the median call time
+    over calls that together take about min_seconds / repeats."""
+    import oracle
+    sub = w.scaled(x.shape[0])
+    per = []
+    for _ in range(repeats):
+        t, _n = oracle.time_topk(x, w.k, return_value=w.return_value, nthreads=nthreads,
+                                 min_seconds=min_seconds / repeats)
+        per.append(t)
+    gbs = sorted((sub.bytes_in + sub.bytes_out) / t / 1e9 for t in per)
+    return {"value": round(statistics.median(gbs), 4), "spread": [round(gbs[0], 4), round(gbs[-1], 4)],
+            "repeats": repeats, "ms_per_call": round(statistics.median(per) * 1e3, 3)}
+
+
+def cpu_baseline(w: workloads.Workload, min_seconds: float, max_rows: int = 256, repeats: int = 3):
     """The oracle as it stands on the host cores, on a bounded sample of the
-    workload: whole rows of the batch, as many as take about `min_seconds`."""
+    workload (evenly spread whole rows): all cores (the reported value) and one
+    thread, each timed `repeats` times with the spread of those repeats."""
     import oracle
     cores = oracle.cores()
-    rows = list(range(w.batch))
-    # bound the sample: at most 256 rows (c4 has 16384)
-    if len(rows) > 256:
-        rows = rows[:: max(1, len(rows) // 256)][:256]
+    rows = sample_rows(w, max_rows)
     x = workloads.generate_rows(w, rows)
     oracle.topk(x, w.k, return_value=w.return_value)  # warm
-    t_per_call, reps = oracle.time_topk(x, w.k, return_value=w.return_value, nthreads=0,
-                                        min_seconds=min_seconds)
-    sub = w.scaled(len(rows))
-    gbs = (sub.bytes_in + sub.bytes_out) / t_per_call / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{len(rows)} of {w.batch} rows of {w.name}, {reps} repeats "
-                      f"({t_per_call * 1e3:.1f} ms per repeat, all {cores} host threads)",
-            "rows_per_s": round(len(rows) / t_per_call, 2)}
+    allc = _oracle_gbs(w, x, 0, min_seconds, repeats)
+    # one thread on at most 32 of the sampled rows
+    x1 = x[: min(32, x.shape[0])].contiguous()
+    one = _oracle_gbs(w, x1, 1, min_seconds, repeats)
+    return {"value": allc["value"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(rows)} of {w.batch} rows of {w.name} (evenly spread), all {cores} host "
+                      f"threads, {repeats} timed repeats ({allc['ms_per_call']} ms per call); one "
+                      f"thread on the first {x1.shape[0]} of them",
+            "spread": allc["spread"], "repeats": repeats,
+            "single_thread": {"value": one["value"], "unit": "GB/s", "cores": 1, "spread": one["spread"],
+                              "repeats": repeats, "rows": x1.shape[0]},
+            "rows_per_s": round(len(rows) / (allc["ms_per_call"] / 1e3), 2)}
 
 
 def run_reference(args, w):
-    world, rank, local = _dist_setup(args.gpus)
+    """The reference arm: the CPU oracle on the host cores. Each step is one
+    oracle call on a bounded sample of the workload's rows (all host threads);
+    W untimed steps, then K timed ones. Only rank 0 runs it."""
+    import oracle
+    world, rank, _local = _dist_setup()
     if rank != 0:
         return 0
-    cb = cpu_baseline(w, min_seconds=max(2.0, min(20.0, 0.5 * args.steps)))
-    value = cb["value"]
+    rows = sample_rows(w, args.ref_rows)
+    x = workloads.generate_rows(w, rows)
+    sub = w.scaled(len(rows))
+    for _ in range(max(1, args.warmup)):
+        oracle.topk(x, w.k, return_value=w.return_value)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.topk(x, w.k, return_value=w.return_value)
+    sec = time.perf_counter() - t0
+    value = (sub.bytes_in + sub.bytes_out) * args.steps / sec / 1e9
+    cores = oracle.cores()
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": round(sec / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": _config(w, None, args.shift),
-        "cpu_baseline": cb,
-        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {len(rows)} of {w.batch} rows of {w.name} (evenly "
+                                   f"spread), all {cores} host threads"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "note": "reference arm = the CPU oracle (plain sort per row), host cores only",
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def _config(w, copies, shift=0):
+def _config(w, l2_note, shift=0):
     cfg = {"workload": f"{w.name}: {w.description}" + (f"; rows start {shift} element(s) past a 16-byte "
                                                         f"boundary" if shift else ""),
            "batch": w.batch, "len": w.length, "k": w.k,
            "input_dtype": "bf16" if w.dtype == torch.bfloat16 else "fp32",
            "sorted_index": w.sorted_index, "return_value": w.return_value,
            "seed": w.seed, "parallelism": "rows independent; one GPU per rank (weak scaling)"}
-    if copies is not None:
-        cfg["l2"] = copies
+    if l2_note is not None:
+        cfg["l2"] = l2_note
     return cfg
+
+
+class Bench:
+    """One workload resident on the device, its outputs, and the CUDA graphs that
+    replay its steps. Steps rotate over `copies` resident inputs so that each
+    reads a copy not touched for copies - 1 steps (copies = 1 when one input
+    alone exceeds four times L2)."""
+
+    def __init__(self, dstk, w, dev, stream, shift=0, order="workload"):
+        self.dstk, self.w, self.dev, self.stream = dstk, w, dev, stream
+        props = torch.cuda.get_device_properties(dev)
+        l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK
+        self.copies = 1 if w.bytes_in >= 4 * l2 else min(64, math.ceil(4 * l2 / w.bytes_in))
+        x0 = shifted(workloads.generate(w, device=dev), shift)
+        self.xs = [x0] + [shifted(x0.contiguous(), shift) for _ in range(self.copies - 1)]
+        self.l2_note = (f"inputs larger than L2 ({w.bytes_in / 1e6:.0f} MB per step > {l2 / 1e6:.0f} MB)"
+                        if self.copies == 1 else
+                        f"rotating {self.copies} resident input copies ({self.copies * w.bytes_in / 1e6:.0f} MB "
+                        f"> 4x L2 {l2 / 1e6:.0f} MB); each step reads a copy not touched for "
+                        f"{self.copies - 1} steps")
+        self.dt_code = dstk.dtype_code(w.dtype)
+        self.sampling = order == "sample"
+        self.idx = torch.empty((w.batch, w.k), dtype=torch.int32, device=dev)
+        self.vals = (torch.empty((w.batch, w.k), dtype=w.dtype, device=dev)
+                     if (w.return_value or self.sampling) else None)
+        self.flag = torch.zeros(1, dtype=torch.int32, device=dev)
+        if self.sampling:  # one fixed uniform number per row
+            self.u = torch.rand(w.batch, generator=torch.Generator().manual_seed(w.seed)).to(dev)
+            self.tokens = torch.empty(w.batch, dtype=torch.int32, device=dev)
+        rc, self.plan = plan_for(dstk, w, props.multi_processor_count, shift)
+        assert rc == dstk.OK, dstk.status_string(rc)
+        self.kernel = kernel_name(w, self.plan)
+        # kernel launches per step: value order adds a sort, the sampler tail a draw
+        self.launches = self.plan.launches + (1 if int(w.sorted_index) == 2 else 0) + (1 if self.sampling else 0)
+        self.chunk = self.copies * max(1, math.ceil(64 / self.copies))
+        self.graphs = {}
+
+    def step(self, i, stream):
+        d, w = self.dstk, self.w
+        x = self.xs[i % self.copies]
+        if self.sampling:
+            r = d.ds_topk_sample(x.data_ptr(), self.dt_code, w.batch, w.length, w.length, w.k,
+                                 SAMPLE_TEMPERATURE, SAMPLE_TOP_P, self.u.data_ptr(), self.vals.data_ptr(),
+                                 self.idx.data_ptr(), self.tokens.data_ptr(), self.flag.data_ptr(),
+                                 stream.cuda_stream)
+        else:
+            r = d.ds_topk(x.data_ptr(), self.dt_code, w.batch, w.length, w.length, w.k,
+                          int(w.sorted_index), int(w.return_value),
+                          self.vals.data_ptr() if (w.return_value and self.vals is not None) else None,
+                          self.idx.data_ptr(), self.flag.data_ptr(), stream.cuda_stream)
+        if r != d.OK:
+            raise d.DsTopkError(r)
+
+    def warm(self, n):
+        with torch.cuda.stream(self.stream):
+            for i in range(n):
+                self.step(i, self.stream)
+        self.stream.synchronize()
+
+    def graph(self, n):
+        """A CUDA graph of n steps (starting at copy 0), replayed once before use
+        so that no timed replay is a graph's first."""
+        if n not in self.graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                for i in range(n):
+                    self.step(i, torch.cuda.current_stream())
+            g.replay()
+            self.stream.synchronize()
+            self.graphs[n] = g
+        return self.graphs[n]
+
+    def replay(self, steps):
+        """Enqueue exactly `steps` steps (whole chunks, then the remainder)."""
+        full, rem = divmod(steps, self.chunk)
+        g_full = self.graph(self.chunk) if full else None
+        g_rem = self.graph(rem) if rem else None
+        return lambda: ([g_full.replay() for _ in range(full)], g_rem.replay() if g_rem else None)
+
+    def time_steps(self, steps, world=1, sampler=None):
+        """Device seconds of exactly `steps` steps, bracketed by a barrier and a
+        device synchronize on both sides (CUDA events on the launching stream)."""
+        go = self.replay(steps)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _barrier(world)
+        torch.cuda.synchronize(self.dev)
+        with torch.cuda.stream(self.stream):
+            ev0.record(self.stream)
+            go()
+            ev1.record(self.stream)
+        self.stream.synchronize()
+        torch.cuda.synchronize(self.dev)
+        _barrier(world)
+        return ev0.elapsed_time(ev1) / 1e3
+
+    def per_step_estimate(self):
+        return self.time_steps(self.chunk) / self.chunk
+
+    def roofline(self, seconds, steps, name):
+        w = self.w
+        bytes_step = w.bytes_in + w.bytes_out
+        # one step's bytes over one launch's share of the step time
+        per_launch_s = seconds / (steps * self.plan.launches)
+        achieved = bytes_step / self.plan.launches / per_launch_s / 1e9
+        peak, peak_src = measured_peak()
+        traffic, traffic_note = profiled_traffic(name, self.kernel)
+        return {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "peak_source": peak_src + (" (of measured)" if peak_src != "fallback" else " (of fallback)"),
+                "traffic": traffic, "traffic_note": traffic_note,
+                "kernel": self.kernel, "kernel_hash": kernel_hash(self.kernel)}
+
+    def free(self):
+        self.graphs.clear()
+        self.xs = None
+        torch.cuda.synchronize(self.dev)
+        torch.cuda.empty_cache()
+
+
+def run_extra(dstk, w, dev, stream, args):
+    """One more workload in the same line: timed over at least args.min_ms of
+    device work (exact step count reported), with its roofline and oracle baseline."""
+    b = Bench(dstk, w, dev, stream, 0, "workload")
+    b.warm(max(3, args.warmup))
+    est = b.per_step_estimate()
+    steps = max(args.steps, min(200000, math.ceil(args.min_ms / 1e3 / est)))
+    sec = b.time_steps(steps)
+    out = {"workload": f"{w.name}: {w.description}", "steps": steps,
+           "ms_per_step": round(sec / steps * 1e3, 6),
+           "value": round(aggregate_value(w.bytes_in + w.bytes_out, steps, 1, sec), 3), "unit": "GB/s",
+           "rows_per_s": round(w.batch * steps / sec, 1), "l2": b.l2_note,
+           "roofline": b.roofline(sec, steps, w.name), "plan": b.plan.as_dict(),
+           "gpu_launches": steps * b.launches}
+    b.free()
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, min_seconds=args.cpu_seconds / 2)
+    return out
 
 
 def run_ours(args, w):
     import sampler_topk_selection_ds_b300 as dstk
 
-    world, rank, local = _dist_setup(args.gpus)
+    world, rank, local = _dist_setup()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK
-
-    # resident inputs: enough copies that one step's input is cold in L2
-    copies = 1 if w.bytes_in >= 4 * l2 else min(64, math.ceil(4 * l2 / w.bytes_in))
-    x0 = shifted(workloads.generate(w, device=dev), args.shift)
-    xs = [x0] + [shifted(x0.contiguous(), args.shift) for _ in range(copies - 1)]
-    l2_note = (f"inputs larger than L2 ({w.bytes_in / 1e6:.0f} MB per step > {l2 / 1e6:.0f} MB)"
-               if copies == 1 else
-               f"rotating {copies} resident input copies ({copies * w.bytes_in / 1e6:.0f} MB > 4x L2 "
-               f"{l2 / 1e6:.0f} MB); each step reads a copy not touched for {copies - 1} steps")
-    dt_code = dstk.dtype_code(w.dtype)
-    idx = torch.empty((w.batch, w.k), dtype=torch.int32, device=dev)
-    vals = torch.empty((w.batch, w.k), dtype=w.dtype, device=dev) if w.return_value else None
-    flag = torch.zeros(1, dtype=torch.int32, device=dev)
-    rc, plan = plan_for(dstk, w, props.multi_processor_count, args.shift)
-    assert rc == dstk.OK, dstk.status_string(rc)
-
-    sampling = args.order == "sample"
-    if sampling:  # the sampler tail needs the values; one fixed uniform number per row
-        vals = torch.empty((w.batch, w.k), dtype=w.dtype, device=dev)
-        u_dev = torch.rand(w.batch, generator=torch.Generator().manual_seed(w.seed)).to(dev)
-        tokens = torch.empty(w.batch, dtype=torch.int32, device=dev)
-
-    def step(i, stream):
-        if sampling:
-            r = dstk.ds_topk_sample(xs[i % copies].data_ptr(), dt_code, w.batch, w.length, w.length, w.k,
-                                    SAMPLE_TEMPERATURE, SAMPLE_TOP_P, u_dev.data_ptr(), vals.data_ptr(),
-                                    idx.data_ptr(), tokens.data_ptr(), flag.data_ptr(), stream.cuda_stream)
-        else:
-            r = dstk.ds_topk(xs[i % copies].data_ptr(), dt_code, w.batch, w.length, w.length, w.k,
-                             int(w.sorted_index), int(w.return_value),
-                             vals.data_ptr() if vals is not None else None, idx.data_ptr(),
-                             flag.data_ptr(), stream.cuda_stream)
-        if r != dstk.OK:
-            raise dstk.DsTopkError(r)
-
     stream = torch.cuda.Stream(dev)
+    name = w.name + (f"+shift{args.shift}" if args.shift else "")
+
+    b = Bench(dstk, w, dev, stream, args.shift, args.order)
     warmup = max(3, args.warmup)
-    with torch.cuda.stream(stream):
-        for i in range(warmup):
-            step(i, stream)
-    stream.synchronize()
-
-    # CUDA graphs of `chunk` steps (a multiple of the rotation) + a remainder graph
-    chunk = copies * max(1, math.ceil(64 / copies))
-    full, rem = divmod(args.steps, chunk)
-
-    def capture(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                step(i, torch.cuda.current_stream())
-        return g
-
-    g_full = capture(chunk) if full else None
-    g_rem = capture(rem) if rem else None
-    if g_full is not None:
-        g_full.replay()
-    stream.synchronize()
-
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b.warm(warmup)
+    b.replay(args.steps)  # capture and replay once every graph the timed region uses
     sampler = ClockSampler(local)
     with sampler:
-        _barrier(world)
-        torch.cuda.synchronize(dev)
-        t_wall0 = time.time()
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(full):
-                g_full.replay()
-            if g_rem is not None:
-                g_rem.replay()
-            ev1.record(stream)
-        stream.synchronize()
-        torch.cuda.synchronize(dev)
-        _barrier(world)
-        t_wall1 = time.time()
-    seconds = ev0.elapsed_time(ev1) / 1e3
+        seconds = b.time_steps(args.steps, world)
     max_seconds = _max_over_ranks(seconds, world)
-    clocks = sampler.summary(t_wall0, t_wall1)
-
+    clocks = sampler.summary()
     bytes_step = w.bytes_in + w.bytes_out
     value = aggregate_value(bytes_step, args.steps, world, max_seconds)
-    # value order adds a sort, the sampler tail a draw
-    launches = plan.launches + (1 if int(w.sorted_index) == 2 else 0) + (1 if sampling else 0)
-    # one step's bytes over one step's device time (all of its launches)
-    per_launch_s = seconds / (args.steps * plan.launches)
-    achieved = bytes_step / plan.launches / per_launch_s / 1e9
-    peak, peak_src = measured_peak()
-    traffic, traffic_note = profiled_traffic(w.name + (f"+shift{args.shift}" if args.shift else ""),
-                                             kernel_name(w, plan))
+    roof = b.roofline(seconds, args.steps, name)
+    # the same steps over at least --min-ms of device work: a check that the
+    # K-step figure is not an artefact of a short timed region
+    est = b.per_step_estimate()
+    long_steps = max(args.steps, min(200000, math.ceil(args.min_ms / 1e3 / est)))
+    long_sec = b.time_steps(long_steps)
+    long_run = {"steps": long_steps, "ms_per_step": round(long_sec / long_steps * 1e3, 6),
+                "value": round(aggregate_value(bytes_step, long_steps, 1, long_sec), 3)}
+    l2_note, plan, launches = b.l2_note, b.plan, b.launches
+    b.free()
 
     # end to end through the public API with host buffers (pinned), copies inside
     e2e = e2e_measure(w, dstk, dev, stream, min(args.steps, args.e2e_steps), args.shift)
+    per_workload = {}
+    if world == 1 and not args.no_extra and args.shift == 0 and args.order == "workload":
+        for extra in EXTRA_WORKLOADS:
+            if extra != w.name:
+                per_workload[extra] = run_extra(dstk, workloads.WORKLOADS[extra], dev, stream, args)
     cb = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(w, min_seconds=args.cpu_seconds)
@@ -420,20 +537,18 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "u16" if w.dtype == torch.bfloat16 else "u32",
             "data": "synthetic (seeded SplitMix64 + Box-Muller, workloads.py)",
-            "config": dict(_config(w, l2_note, args.shift), **({"call": f"ds_topk_sample (temperature {SAMPLE_TEMPERATURE}, "
-                                                           f"top_p {SAMPLE_TOP_P})"} if sampling else {})),
+            "config": dict(_config(w, l2_note, args.shift),
+                           **({"call": f"ds_topk_sample (temperature {SAMPLE_TEMPERATURE}, top_p {SAMPLE_TOP_P})"}
+                              if args.order == "sample" else {})),
             "rows_per_s": round(w.batch * args.steps * world / max_seconds, 1),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
-                         "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "peak_source": peak_src + (" (of measured)" if peak_src != "fallback" else " (of fallback)"),
-                         "traffic": traffic, "traffic_note": traffic_note,
-                         "kernel": kernel_name(w, plan),
-                         "kernel_hash": kernel_hash(kernel_name(w, plan))},
+            "roofline": roof,
+            "long_run": long_run,
             "e2e": e2e,
             "gpu_launches": args.steps * launches,
             "plan": plan.as_dict(),
             "clocks": clocks,
             "cpu_baseline": cb,
+            "per_workload": per_workload or None,
             "gpu": props.name,
         }
         print(json.dumps(line), flush=True)
@@ -499,13 +614,18 @@ def run_case(args, w):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--min-ms", type=float, default=100.0,
+                    help="device time of the long check run and of each per-workload run")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=6.0)
+    ap.add_argument("--ref-rows", type=int, default=64,
+                    help="--impl reference: rows of the workload per oracle step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--order", default="workload", choices=["workload", "value", "sample"],
                     help="value: value-ordered output (sorted_index 2; one more launch per call); "
                          "sample: the sampler tail ds_topk_sample (temperature 1, top_p 0.9; "

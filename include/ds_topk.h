@@ -60,7 +60,8 @@ typedef enum {
 
 /* Bits the kernels OR into *nan_flag (the device status word). */
 #define DS_TOPK_FLAG_NAN 1     /* some row held a NaN in [0, len)                        */
-#define DS_TOPK_FLAG_TIMEOUT 2 /* a bounded device-side wait gave up (never expected)     */
+#define DS_TOPK_FLAG_TIMEOUT 2 /* a bounded device-side wait gave up (never expected);
+                                  every output of the call is then undefined          */
 
 /* Hard limit on k, from the pages ("topk <= 4096"). */
 #define DS_TOPK_MAX_K 4096
@@ -86,7 +87,9 @@ typedef enum {
  *                16-byte boundary (x 16-byte aligned and row_stride *
  *                sizeof(dtype) a multiple of 16) take the fast paths; any other
  *                rows take DS_TOPK_PATH_UNALIGNED, which gives the same result
- *                more slowly (it re-reads each row once per 8-bit key digit).
+ *                more slowly (one CTA per row; the row is read once to filter
+ *                candidates against a guessed threshold, and again from L2 only
+ *                when the guess fails or for the ordered output).
  *   dtype        DS_TOPK_BF16 or DS_TOPK_FP32.
  *   batch        number of rows, >= 0. batch == 0 returns DS_TOPK_OK at once
  *                (pointers may then be NULL).
@@ -185,7 +188,9 @@ DS_TOPK_API int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len,
  *   out_tokens   device pointer [batch] int32, 4-byte aligned: the drawn column.
  * The arithmetic is fp32 (expf and sums over the k survivors); a draw can
  * differ from an exact (float64) computation only when u * C_m or
- * top_p * C_{k-1} lies within about (k + 2) * 2^-23 * C_{k-1} of a step of C.
+ * top_p * C_{k-1} lies within (k + 40) * 2^-22 * C_{k-1} of a step of C (expf
+ * within 2 ulp, the rounded argument, a block scan of depth at most 40 and the
+ * two products; the tests check the draws against exactly this bound).
  * A row holding a NaN gets an unspecified but in-range token.
  * Returns DS_TOPK_OK, DS_TOPK_EINVAL (also for a bad temperature or top_p),
  * DS_TOPK_EALIGN or DS_TOPK_ECUDA, like ds_topk; nothing is enqueued on an
@@ -202,8 +207,10 @@ typedef enum {
   DS_TOPK_PATH_WARP_ROWS = 2, /* one warp per row, several rows per CTA: many rows of at
                                  most 65536 elements with k <= 1024                  */
   DS_TOPK_PATH_UNALIGNED = 3   /* one CTA per row for rows that do not start on a
-                                  16-byte boundary: exact radix selection, 8 bits of
-                                  the order key per pass over the row              */
+                                  16-byte boundary: candidates filtered against a
+                                  guessed threshold into shared memory and radix-
+                                  selected there (exact radix levels over the whole
+                                  row when the guess fails)                        */
 } ds_topk_path;
 
 /* Launch plan of one ds_topk call, as chosen by the host dispatcher. */
@@ -215,10 +222,11 @@ typedef struct {
                                   (1 on DS_TOPK_PATH_WARP_ROWS and
                                   DS_TOPK_PATH_UNALIGNED: vectors are tested one by one) */
   int64_t grid_ctas;           /* CTAs if every row had its own cluster (warp rows: if
-                                  every 8 rows had their own CTA); ds_topk launches at
-                                  most as many as can be co-resident, and each
-                                  persistent cluster (warp) then walks rows with a
-                                  stride                                               */
+                                  every 8 rows had their own CTA), capped at INT32_MAX
+                                  on the warp-rows and unaligned-rows paths; ds_topk
+                                  launches at most as many as can be co-resident, and
+                                  each persistent cluster (warp) then walks rows with
+                                  a stride                                             */
   int64_t granules_per_cta;    /* size of the per-CTA granule-maximum array; on
                                   DS_TOPK_PATH_WARP_ROWS the candidate slots per warp,
                                   on DS_TOPK_PATH_UNALIGNED the candidate slots per CTA */

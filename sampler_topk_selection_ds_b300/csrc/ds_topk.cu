@@ -101,7 +101,9 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
     // the first-row sample)
     int64_t cap = 4 * static_cast<int64_t>(k) + 2048;
     if (cap < ds_topk_dev::kUaSampleKeys) cap = ds_topk_dev::kUaSampleKeys;
-    pl.grid_ctas = batch;
+    // persistent: each CTA walks rows with a stride of the grid, so the grid may
+    // be capped at the largest launchable size
+    pl.grid_ctas = batch < INT32_MAX ? batch : INT32_MAX;
     pl.granules_per_cta = cap;
     pl.smem_bytes = static_cast<int32_t>(cap * 4);
     pl.launches = batch > 0 ? 1 : 0;
@@ -151,7 +153,10 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
       pl.cluster_size = 1;
       pl.threads_per_cta = ds_topk_dev::kWrThreads;
       pl.vectors_per_granule = 1;
+      // persistent: each warp walks rows with a stride of all warps, so the grid
+      // may be capped at the largest launchable size
       pl.grid_ctas = ceil_div(batch, ds_topk_dev::kWrWarps);
+      if (pl.grid_ctas > INT32_MAX) pl.grid_ctas = INT32_MAX;
       pl.granules_per_cta = cap;
       pl.smem_bytes = static_cast<int32_t>(smem);
       pl.launches = 1;
@@ -611,7 +616,6 @@ extern "C" int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, 
     // every resident CTA walks rows with a stride of the grid
     const int resident_ctas = resident_cached(dev_id, pl, dev.sm_count);
     if (resident_ctas > 0 && pl.pub.grid_ctas > resident_ctas) pl.pub.grid_ctas = resident_ctas;
-    if (pl.pub.grid_ctas > INT32_MAX) pl.pub.grid_ctas = INT32_MAX;
     const cudaError_t e = es == 2 ? launch_dtype<2>(pl, stream) : launch_dtype<4>(pl, stream);
     if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) {
       cudaGetLastError();

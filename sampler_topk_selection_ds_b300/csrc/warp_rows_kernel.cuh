@@ -54,7 +54,11 @@ constexpr int kWrSampleBlocks = 16;        // first-row sample: 16 blocks of 32 
 constexpr int kWrChunk = 2048;             // bytes per bulk copy of a row (128 vectors)
 constexpr int kWrChunkVecs = kWrChunk / 16;
 constexpr int kWrMaxDepth = 3;             // chunks in flight per warp
-constexpr uint32_t kWrWaitLimit = 1u << 22;  // bounded mbarrier polls
+// Bounded mbarrier polls (a test build sets a short limit to make a wait run out).
+#ifndef DS_TOPK_WAIT_LIMIT
+#define DS_TOPK_WAIT_LIMIT (1u << 22)
+#endif
+constexpr uint32_t kWrWaitLimit = DS_TOPK_WAIT_LIMIT;
 constexpr uint32_t kWrSuspendNs = 1000;      // a poll may sleep this long before it fails
 
 struct WrParams {

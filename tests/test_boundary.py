@@ -182,3 +182,34 @@ def test_bench_kernel_hash_ignores_comments_only():
     hashes = {bench.kernel_hash(k) for k in ("topk_rows_kernel<4,4>", "topk_warp_rows_kernel<2>",
                                              "topk_unaligned_kernel<2>")}
     assert len(hashes) == 3
+
+
+def test_bench_traffic_table():
+    """bench.py reads each workload's measured DRAM traffic from a JSON data file;
+    a figure counts only for the kernel (and kernel code) it was measured on."""
+    import json
+
+    import bench
+    with open(os.path.join(bench.ROOT, bench.TRAFFIC_FILE), encoding="utf-8") as fh:
+        table = json.load(fh)
+    assert table
+    for wl, e in table.items():
+        assert {"kernel", "kernel_hash", "dram_bytes_per_launch", "summary"} <= set(e)
+        assert os.path.exists(os.path.join(bench.ROOT, e["summary"])), e["summary"]
+        t, note = bench.profiled_traffic(wl, e["kernel"])
+        if e["kernel_hash"] == bench.kernel_hash(e["kernel"]):
+            assert t == e["dram_bytes_per_launch"]
+        else:
+            assert t is None and note.startswith("stale")
+        other = "topk_unaligned_kernel<2>" if not e["kernel"].startswith("topk_unaligned") else "topk_rows_kernel<4,4>"
+        assert bench.profiled_traffic(wl, other)[0] is None
+    assert bench.profiled_traffic("no-such-workload", "topk_rows_kernel<4,4>")[0] is None
+
+
+def test_bench_sample_rows_bounded():
+    import bench
+    import workloads
+    c4 = workloads.WORKLOADS["c4"]
+    rows = bench.sample_rows(c4, 256)
+    assert len(rows) == 256 and rows[0] == 0 and rows[-1] < c4.batch and rows == sorted(set(rows))
+    assert bench.sample_rows(workloads.WORKLOADS["c2"], 256) == list(range(64))

@@ -3,8 +3,13 @@
 The selection part (the k survivors, their values and value order) must be
 bit-exact. The draw runs in fp32 on the GPU and in float64 in the oracle, so a
 drawn position may differ only where floating point decides it: where the
-oracle's cumulative weights C put a step within the fp32 bound
-(k + 2) * 2^-23 * C_{k-1} (exp and a k-term sum) of u * C_m or of the top-p mass.
+oracle's cumulative weights C put a step within tol(k) = (k + 40) * 2^-22 *
+C_{k-1} of u * C_m or of the top-p mass. With u = 2^-24 the fp32 unit roundoff:
+each weight is off by at most 4u w_j + 1.2u (expf within 2 ulp, and an argument
+(v_j - v_0) / T rounded three times, whose effect w |a| 3u is at most 3u / e);
+every prefix sum of the block scan by at most 40u C_{k-1} beyond that; the
+products u * C_m and top_p * C_{k-1} by u C_{k-1} each. Both sides of one
+comparison together: (1.2 k + 45) * 2^-23 * C_{k-1} <= tol(k).
 Every other row must draw the same token.
 """
 import numpy as np
@@ -29,7 +34,7 @@ def _cuda():
 def _near_boundary(v, temperature, top_p, u, gpu_pos):
     w = osam.weights(v, temperature)
     c = np.cumsum(w)
-    tol = 4 * (len(v) + 2) * 2.0 ** -23 * c[-1]  # fp32 bound, with a factor 4 of slack
+    tol = (len(v) + 40) * 2.0 ** -22 * c[-1]  # the fp32 bound derived above
     m_exact = int(np.argmax(c >= top_p * c[-1]))
     ms = {m_exact} | {int(m) for m in np.nonzero(np.abs(c - top_p * c[-1]) <= tol)[0]}
     for m in ms:

@@ -175,10 +175,11 @@ def test_unaligned_c2_shape_full():
     check(x, w.k, 1, w.length, w.sorted_index, w.return_value)
 
 
-def test_unaligned_c4_shape_sampled():
+def test_unaligned_c4_shape_full():
     """The decode workload's shape (16384 x 32768 bf16, k = 512) one element off
-    the 16-byte boundary, as the benchmark's shifted mode times it: the oracle on
-    sampled rows, properties on every row."""
+    the 16-byte boundary, as the benchmark's shifted mode times it: every row
+    against the oracle."""
+    from tests.test_gpu_parity import assert_rows_equal_oracle
     w = workloads.WORKLOADS["c4"]
     xd = workloads.generate(w, device="cuda")
     buf = torch.empty(w.batch * w.length + 8, dtype=xd.dtype, device="cuda")
@@ -187,9 +188,6 @@ def test_unaligned_c4_shape_sampled():
     del xd
     gv, gi, gf = run_view(view, w.k, w.sorted_index, w.return_value)
     assert gv is None and gf == 0
-    rows = sorted(set([0, 1, 2, w.batch - 1] + list(range(5, w.batch, w.batch // 40))))
-    x_rows = view[rows].cpu()
-    assert_parity(x_rows, w.k, w.sorted_index, w.return_value, gpu_out=(None, gi[rows], gf))
-    s = torch.sort(gi.to(torch.int64), dim=1).values
-    assert (s[:, 1:] > s[:, :-1]).all()
-    assert s.min().item() >= 0 and s.max().item() < 24576  # never from the -inf tail
+    x = view.cpu()
+    del buf, view
+    assert_rows_equal_oracle(x, w.k, gi)
