@@ -13,23 +13,27 @@
 //     maxima (16 evenly spaced blocks of 32 vectors). t is only a guess; the
 //     step below checks it.
 //  S  stream the row once through a per-warp shared-memory ring of 2 KB bulk
-//     async copies (lane v mod 32 reads vector v from it); a vector whose
-//     NaN-propagating maximum reaches t is listed (ballot + popc, so the list
-//     stays in index order) and its data parked in a small shared-memory ring.
-//     Every 32 listed vectors the warp extracts their elements >= t (or NaN) as
-//     candidates, again in index order. The guess holds iff k <= candidates <=
-//     capacity: then the candidates contain the row's top k.
-//  R  exact k-th key K* among the candidates: 256-bin histogram levels over
-//     the key range [t, max], each level narrowing the range by 8 bits.
+//     async copies. In each chunk lane j owns 4 consecutive 16-byte vectors
+//     (64 contiguous bytes); it marks its elements >= t (or NaN) in one 32-bit
+//     mask with packed compares, one warp prefix sum over the lanes' counts
+//     places the chunk's candidates, and each lane copies its marked elements
+//     (read back from the chunk in shared memory) into the warp's candidate
+//     buffer. Lanes own consecutive vectors, so candidates land in index order.
+//     The guess holds iff k <= candidates <= capacity (and no NaN): then the
+//     candidates contain the row's top k.
+//  R  exact k-th key K* among the candidates: 256-bin histogram levels, the
+//     first over the 256 top-16-bit keys from t up (it also spots a NaN),
+//     each further level narrowing the range by 8 bits.
 //  C  one ordered pass over the candidates: keep key > K*, and keys == K*
 //     while their running count stays below the ties still needed; outputs
 //     are written in ascending index order (sorted_index costs nothing).
 //
 // A row whose guess fails is retried (sample threshold, a sample rank adapted to
-// the count seen, the exact k-th vector maximum); a row that still fails
-// (massive ties, a NaN, k above the number of finite vectors) takes the exact
-// fallback: 8-bit radix levels over every element of the row, then one ordered
-// output pass. Rows with a NaN set the device flag there.
+// the count seen, the exact k-th vector maximum) with direct passes over the
+// row; a row that still fails (massive ties, a NaN, k above the number of
+// finite vectors) takes the exact fallback: 8-bit radix levels over every
+// element of the row, then one ordered output pass. Rows with a NaN set the
+// device flag there.
 //
 // Sources: deepseek.csdn.net, "DeepSeek 一次开源三个仓库", section 三 (算子层):
 // the threshold filter into a candidate buffer and its compaction to K;
@@ -46,13 +50,12 @@ namespace ds_topk_dev {
 
 constexpr int kWrWarps = 8;                // rows in flight per CTA
 constexpr int kWrThreads = 32 * kWrWarps;
-constexpr int kWrU = 4;                    // 16-byte loads in flight per lane (direct passes)
 constexpr int kWrMaxLen = 65536;           // candidate indices are kept in 16 bits
 constexpr int kWrMaxK = 1024;
-constexpr int kWrRing = 64;                // listed vectors parked per warp
 constexpr int kWrSampleBlocks = 16;        // first-row sample: 16 blocks of 32 vectors
 constexpr int kWrChunk = 2048;             // bytes per bulk copy of a row (128 vectors)
 constexpr int kWrChunkVecs = kWrChunk / 16;
+constexpr int kWrLaneVecs = kWrChunkVecs / 32;  // consecutive vectors a lane owns per chunk
 constexpr int kWrMaxDepth = 3;             // chunks in flight per warp
 // Bounded mbarrier polls (a test build sets a short limit to make a wait run out).
 #ifndef DS_TOPK_WAIT_LIMIT
@@ -60,6 +63,8 @@ constexpr int kWrMaxDepth = 3;             // chunks in flight per warp
 #endif
 constexpr uint32_t kWrWaitLimit = DS_TOPK_WAIT_LIMIT;
 constexpr uint32_t kWrSuspendNs = 1000;      // a poll may sleep this long before it fails
+
+static_assert(kWrLaneVecs == 4, "a lane's candidate mask holds 4 vectors of 8 bf16 elements");
 
 struct WrParams {
   const char* x;
@@ -77,11 +82,10 @@ struct WrParams {
   int32_t* flag;
 };
 
-// Per-warp shared memory: streaming ring (depth x 2 KB) | ring of listed vectors
-// (also the 256-bin histogram: the two are never live at once) | their vector
-// indices | mbarriers | candidate words | candidate indices (fp32 only). bf16
-// candidate word: input bits | index << 16; fp32: input bits, index apart.
-constexpr int kWrFixedBytes = kWrRing * 16 + kWrRing * 2 + 32;
+// Per-warp shared memory: streaming ring (depth x 2 KB) | 256-bin histogram |
+// mbarriers | candidate words | candidate indices (fp32 only). bf16 candidate
+// word: input bits | index << 16; fp32: input bits, index apart.
+constexpr int kWrFixedBytes = kRadix * 4 + kWrMaxDepth * 8 + 8;
 __host__ __device__ constexpr int64_t wr_warp_bytes(int es, int64_t cap, int depth) {
   return depth * kWrChunk + kWrFixedBytes + cap * 4 + (es == 4 ? cap * 2 : 0);
 }
@@ -99,27 +103,6 @@ __device__ __forceinline__ uint32_t vec_max(const uint4& w) {
   } else {
     return f32_max_nan(f32_max_nan(w.x, w.y), f32_max_nan(w.z, w.w));
   }
-}
-
-// Ballot over the warp of "some element of the lane's vector reaches the
-// threshold (or is NaN)", for lanes with `in` set.
-template <int ES>
-__device__ __forceinline__ uint32_t ballot_reaches(uint32_t vmax, float tval, uint32_t tv2, bool in) {
-  uint32_t b;
-  if constexpr (ES == 2) {
-    asm volatile(
-        "{\n\t.reg .pred lo, hi, q;\n\t"
-        "setp.ne.u32 q, %3, 0;\n\t"
-        "setp.geu.bf16x2 lo|hi, %1, %2;\n\t"
-        "or.pred lo, lo, hi;\n\t"
-        "and.pred lo, lo, q;\n\t"
-        "vote.sync.ballot.b32 %0, lo, 0xffffffff;\n\t}"
-        : "=r"(b) : "r"(vmax), "r"(tv2), "r"(static_cast<uint32_t>(in)));
-  } else {
-    (void)tv2;
-    b = __ballot_sync(0xFFFFFFFFu, in && !(__uint_as_float(vmax) < tval));
-  }
-  return b;
 }
 
 // ---- bulk copies into shared memory, completed through an mbarrier ----------------
@@ -204,6 +187,40 @@ __device__ __forceinline__ void wr_clear_hist(uint32_t* h) {
   __syncwarp();
 }
 
+// Candidate bits of one 16-byte vector against threshold value tval (tv2: its
+// bf16 bits in both halves): bit e set iff element e is not below the threshold
+// or is NaN (unordered compares), so every NaN becomes a candidate and is seen
+// by the selection. bf16: 8 bits from 4 packed compares (setp.geu.bf16x2 sets
+// the first predicate from the low half, i.e. the even element); fp32: 4 bits.
+template <int ES>
+__device__ __forceinline__ uint32_t vec_cand_bits(const uint4& w, float tval, uint32_t tv2) {
+  uint32_t m;
+  if constexpr (ES == 2) {
+    (void)tval;
+    asm("{\n\t.reg .pred a0, a1, b0, b1, c0, c1, d0, d1;\n\t"
+        "setp.geu.bf16x2 a0|a1, %1, %5;\n\t"
+        "setp.geu.bf16x2 b0|b1, %2, %5;\n\t"
+        "setp.geu.bf16x2 c0|c1, %3, %5;\n\t"
+        "setp.geu.bf16x2 d0|d1, %4, %5;\n\t"
+        "selp.u32 %0, 1, 0, a0;\n\t"
+        "@a1 or.b32 %0, %0, 2;\n\t"
+        "@b0 or.b32 %0, %0, 4;\n\t"
+        "@b1 or.b32 %0, %0, 8;\n\t"
+        "@c0 or.b32 %0, %0, 16;\n\t"
+        "@c1 or.b32 %0, %0, 32;\n\t"
+        "@d0 or.b32 %0, %0, 64;\n\t"
+        "@d1 or.b32 %0, %0, 128;\n\t}"
+        : "=r"(m) : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(tv2));
+  } else {
+    (void)tv2;
+    m = static_cast<uint32_t>(!(__uint_as_float(w.x) < tval)) |
+        static_cast<uint32_t>(!(__uint_as_float(w.y) < tval)) << 1 |
+        static_cast<uint32_t>(!(__uint_as_float(w.z) < tval)) << 2 |
+        static_cast<uint32_t>(!(__uint_as_float(w.w) < tval)) << 3;
+  }
+  return m;
+}
+
 template <int ES>
 struct WarpRow {
   using T = Traits<ES>;
@@ -213,28 +230,26 @@ struct WarpRow {
 
   const WrParams& p;
   uint4* chunks;  // streaming ring, depth x kWrChunkVecs vectors
-  uint4* ring;    // listed vectors
-  uint16_t* ring_v;
   uint32_t* hist;
   uint64_t* mbar;
   uint32_t* cw;   // candidate words
   uint16_t* ci;   // candidate indices (fp32)
   int lane;
   uint32_t lt;
+  int rot;        // rotation of the lane's four loads (conflict-free shared-memory reads)
   int nfull;      // vectors wholly inside a row
   int nch;        // bulk chunks per row (they cover the nfull whole vectors)
 
   __device__ WarpRow(const WrParams& prm, unsigned char* base)
       : p(prm),
         chunks(reinterpret_cast<uint4*>(base)),
-        ring(reinterpret_cast<uint4*>(base + prm.depth * kWrChunk)),
-        ring_v(reinterpret_cast<uint16_t*>(base + prm.depth * kWrChunk + kWrRing * 16)),
         hist(reinterpret_cast<uint32_t*>(base + prm.depth * kWrChunk)),
-        mbar(reinterpret_cast<uint64_t*>(base + prm.depth * kWrChunk + kWrRing * 18)),
+        mbar(reinterpret_cast<uint64_t*>(base + prm.depth * kWrChunk + kRadix * 4)),
         cw(reinterpret_cast<uint32_t*>(base + prm.depth * kWrChunk + kWrFixedBytes)),
         ci(reinterpret_cast<uint16_t*>(base + prm.depth * kWrChunk + kWrFixedBytes) + 2 * prm.cap),
         lane(threadIdx.x & 31),
         lt(lanemask_lt()),
+        rot((threadIdx.x >> 1) & 3),
         nfull(prm.len / VEC),
         nch((prm.len / VEC + kWrChunkVecs - 1) / kWrChunkVecs) {}
 
@@ -320,131 +335,81 @@ struct WarpRow {
     return ES == 2 ? static_cast<int>(cw[pos] >> 16) : static_cast<int>(ci[pos]);
   }
 
-  // ---- S: listing and candidate extraction under a threshold key ------------------
-  struct Lister {
-    float tval;
-    uint32_t tv2;
-    int wpos, rpos, ccount;  // warp-uniform
-    bool nan;                // per lane
-    uint32_t kmax;           // per lane: largest key of the lane's listed vectors
-  };
-  __device__ __forceinline__ Lister lister(uint32_t tk) const {
-    Lister L;
-    L.tval = key_threshold_value<ES>(tk);
-    L.tv2 = (__float_as_uint(L.tval) >> 16) * 0x00010001u;
-    L.wpos = L.rpos = L.ccount = 0;
-    L.nan = false;
-    L.kmax = 0;
-    return L;
+  // ---- S: candidates of a group of 32 x 4 consecutive vectors ---------------------
+  // M: the lane's candidate mask over its 4 consecutive vectors (bit VEC*v + e:
+  // element e of the lane's vector v); ibase: the row index of the lane's first
+  // element. The lanes' candidates are appended at *ccount (warp-uniform) in
+  // index order (writes stop at cap; the count does not). bits_of(b) returns
+  // the element bits behind mask bit b.
+  template <typename BitsOf>
+  __device__ __forceinline__ void emit(uint32_t M, int ibase, int* ccount, BitsOf bits_of) const {
+    if (__ballot_sync(kFull, M != 0u) == 0u) return;  // warp-uniform: nothing here
+    const uint32_t cnt = __popc(M);
+    const uint32_t excl = warp_excl_scan(cnt);
+    const int tot = static_cast<int>(__shfl_sync(kFull, excl + cnt, 31));
+    int pos = *ccount + static_cast<int>(excl);
+    while (M) {
+      const int b = __ffs(M) - 1;
+      M &= M - 1;
+      if (pos < p.cap) put(pos, bits_of(b), ibase + b);
+      ++pos;
+    }
+    *ccount += tot;
   }
 
-  // Elements >= t (or NaN) of `cnt` listed vectors starting at ring slot L.rpos
-  // (one vector per lane), appended in index order at candidate position
-  // L.ccount (writes stop at cap). Every element slot is written by a static,
-  // predicated store, so lanes never diverge.
-  __device__ __forceinline__ void extract(Lister& L, int cnt) const {
-    const bool has = lane < cnt;
-    const int slot = (L.rpos + lane) & (kWrRing - 1);
+  // Candidate mask of the lane's 4 consecutive vectors held in r[0..3], where
+  // r[u] is the lane's vector vu(u) (0..3) and only vectors below `valid` count.
+  __device__ __forceinline__ uint32_t lane_mask(const uint4 (&r)[kWrLaneVecs], const int (&vu)[kWrLaneVecs],
+                                                int valid, float tval, uint32_t tv2) const {
+    uint32_t M = 0;
+#pragma unroll
+    for (int u = 0; u < kWrLaneVecs; ++u) {
+      const uint32_t b = vec_cand_bits<ES>(r[u], tval, tv2);
+      M |= (vu[u] < valid ? b : 0u) << (VEC * vu[u]);
+    }
+    return M;
+  }
+
+  // Element bits behind mask bit b of the lane's 4 vectors, from registers (the
+  // retry passes, which read the row straight from global memory).
+  __device__ __forceinline__ static uint32_t reg_bits(const uint4 (&r)[kWrLaneVecs], int b) {
+    const int v = b / VEC, e = b % VEC;
+    const uint4 a = (v & 2) ? ((v & 1) ? r[3] : r[2]) : ((v & 1) ? r[1] : r[0]);
+    return elem_bits<ES>(a, e);
+  }
+
+  // The retry pass: the row straight from global memory (it was just streamed,
+  // so mostly from L2), 4 consecutive vectors per lane. Returns the candidate
+  // count (it may exceed cap; writes stop there).
+  __device__ int direct_pass(const char* rowp, uint32_t tk) const {
+    const float tval = key_threshold_value<ES>(tk);
+    const uint32_t tv2 = (__float_as_uint(tval) >> 16) * 0x00010001u;
+    const int vu[kWrLaneVecs] = {0, 1, 2, 3};
+    int ccount = 0;
+    for (int g = 0; g < nfull; g += kWrChunkVecs) {
+      const int v0 = g + lane * kWrLaneVecs;
+      uint4 r[kWrLaneVecs];
+#pragma unroll
+      for (int u = 0; u < kWrLaneVecs; ++u)
+        r[u] = v0 + u < nfull ? ld_nc_v4(rowp + static_cast<int64_t>(v0 + u) * 16) : make_uint4(0, 0, 0, 0);
+      const uint32_t M = lane_mask(r, vu, nfull - v0, tval, tv2);
+      emit(M, v0 * VEC, &ccount, [&](int b) { return reg_bits(r, b); });
+    }
+    ragged(rowp, tval, tv2, &ccount);
+    return ccount;
+  }
+
+  // The ragged last vector of a row (len not a multiple of VEC): scalar loads,
+  // elements at or past len masked off; its candidates come last in index order.
+  __device__ __forceinline__ void ragged(const char* rowp, float tval, uint32_t tv2, int* ccount) const {
+    if (nfull == p.nvec) return;  // warp-uniform
     uint4 w = make_uint4(0, 0, 0, 0);
-    int v = 0;
     uint32_t m = 0;
-    if (has) {
-      w = ring[slot];
-      v = ring_v[slot];
-      m = cand_mask<ES>(w, L.tval, L.tv2);
-      const int rem = p.len - v * VEC;
-      if (rem < VEC) m &= (1u << rem) - 1u;
-      // a NaN element makes the maximum NaN; otherwise the maximum's key
-      // bounds the keys of the row's candidates from above
-      const uint32_t mx = finish_max<ES>(vec_max<ES>(w));
-      L.nan |= is_nan_bits<ES>(mx);
-      L.kmax = max(L.kmax, key_of<ES>(mx));
+    if (lane == 0) {
+      w = load_vec<ES>(rowp, nfull, p.len);
+      m = vec_cand_bits<ES>(w, tval, tv2) & ((1u << (p.len - nfull * VEC)) - 1u);
     }
-    const uint32_t c = __popc(m);
-    const uint32_t pre = warp_excl_scan(c);
-    const int tot = static_cast<int>(__shfl_sync(kFull, pre + c, 31));
-    int pos = L.ccount + static_cast<int>(pre);
-    const int ib = v * VEC;
-    if (L.ccount + 32 * VEC <= p.cap) {  // warp-uniform: room for a whole round
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-      uint32_t* dst = cw + pos;
-      if constexpr (ES == 2) {
-        // candidate word = element bits | index << 16: one byte permute each
-#pragma unroll
-        for (int e = 0; e < VEC; ++e)
-          if (m & (1u << e)) *dst++ = __byte_perm(ws[e >> 1], static_cast<uint32_t>(ib + e), (e & 1) ? 0x5432 : 0x5410);
-      } else {
-        uint16_t* di = ci + pos;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          if (m & (1u << e)) {
-            *dst++ = ws[e];
-            *di++ = static_cast<uint16_t>(ib + e);
-          }
-        }
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        if (m & (1u << e)) {
-          if (pos < p.cap) put(pos, elem_bits<ES>(w, e), ib + e);
-          ++pos;
-        }
-      }
-    }
-    L.ccount += tot;
-    L.rpos += cnt;
-  }
-
-  // One vector per lane (vector v of the row, valid if `in`): list it if it
-  // reaches the threshold; every 32 listed vectors, extract their candidates.
-  __device__ __forceinline__ void step(Lister& L, const uint4& w, int v, bool in) const {
-    const uint32_t b = ballot_reaches<ES>(vec_max<ES>(w), L.tval, L.tv2, in);
-    if (b == 0u) return;  // warp-uniform: nothing listed in this step
-    if (b & (1u << lane)) {
-      const int slot = (L.wpos + __popc(b & lt)) & (kWrRing - 1);
-      ring[slot] = w;
-      ring_v[slot] = static_cast<uint16_t>(v);
-    }
-    L.wpos += __popc(b);
-    if (L.wpos - L.rpos >= 32) {
-      __syncwarp();
-      extract(L, 32);
-      __syncwarp();
-    }
-  }
-  // Returns the number of candidates (it may exceed cap; writes stop there).
-  __device__ __forceinline__ int finish(Lister& L) const {
-    if (L.wpos > L.rpos) {
-      __syncwarp();
-      extract(L, L.wpos - L.rpos);
-      __syncwarp();
-    }
-    return L.ccount;
-  }
-
-  // The listing pass reading the row directly from global memory (retries).
-  __device__ int direct_pass(const char* rowp, uint32_t tk, bool* nan, uint32_t* kmax) const {
-    Lister L = lister(tk);
-    const int nsteps = (p.nvec + 31) / 32;
-    for (int i0 = 0; i0 < nsteps; i0 += kWrU) {
-      uint4 w[kWrU];
-#pragma unroll
-      for (int u = 0; u < kWrU; ++u) {
-        const int v = (i0 + u) * 32 + lane;
-        w[u] = v < p.nvec ? load(rowp, v) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < kWrU; ++u) {
-        if (i0 + u >= nsteps) break;  // warp-uniform
-        const int v = (i0 + u) * 32 + lane;
-        step(L, w[u], v, v < p.nvec);
-      }
-    }
-    const int n = finish(L);
-    *nan = L.nan;
-    *kmax = __reduce_max_sync(kFull, L.kmax);
-    return n;
+    emit(m, nfull * VEC, ccount, [&](int b) { return elem_bits<ES>(w, b); });
   }
 
   // ---- the streaming ring: chunks of the warp's rows, in order, depth ahead -------
@@ -481,13 +446,17 @@ struct WarpRow {
       st.src += kWrChunk;
     }
   }
-  // The listing pass over one row, fed by the ring: each chunk read frees its
-  // slot for the chunk `depth` places further on. Returns false if a copy never
-  // completed within the poll limit (the warp must then stop).
-  __device__ bool stream_pass(Stream& st, int64_t row_step, const char* rowp, uint32_t tk, int* n,
-                              bool* nan, uint32_t* kmax) const {
-    Lister L = lister(tk);
-    constexpr int kSteps = kWrChunkVecs / 32;
+  // The candidate pass over one row, fed by the ring: a chunk's slot is refilled
+  // with the chunk `depth` places further on once its candidates are copied out.
+  // Returns false if a copy never completed within the poll limit (the warp must
+  // then stop); else the candidate count in *n (it may exceed cap).
+  __device__ bool stream_pass(Stream& st, int64_t row_step, const char* rowp, uint32_t tk, int* n) const {
+    const float tval = key_threshold_value<ES>(tk);
+    const uint32_t tv2 = (__float_as_uint(tval) >> 16) * 0x00010001u;
+    int vu[kWrLaneVecs];
+#pragma unroll
+    for (int u = 0; u < kWrLaneVecs; ++u) vu[u] = (u + rot) & (kWrLaneVecs - 1);
+    int ccount = 0;
     for (int c = 0; c < nch; ++c) {
       const int slot = st.cslot;
       if (!__all_sync(kFull, mbar_wait(mbar + slot, st.cphase))) return false;
@@ -495,36 +464,26 @@ struct WarpRow {
         st.cslot = 0;
         st.cphase ^= 1u;
       }
-      const uint4* buf = chunks + slot * kWrChunkVecs + lane;
-      const int vb = c * kWrChunkVecs + lane;
-      uint4 w[kSteps];
-      if (c < nch - 1 || nfull % kWrChunkVecs == 0) {  // a whole chunk
+      // the lane's 64 bytes; load u reads vector vu[u], so the 8 lanes of each
+      // quarter-warp touch 8 distinct 16-byte bank groups
+      const uint4* lv = chunks + slot * kWrChunkVecs + lane * kWrLaneVecs;
+      const int v0 = c * kWrChunkVecs + lane * kWrLaneVecs;
+      uint4 r[kWrLaneVecs];
 #pragma unroll
-        for (int u = 0; u < kSteps; ++u) w[u] = buf[u * 32];
-        __syncwarp();  // every lane has read the slot: refill it
-        ++st.consumed;
-        produce_one(st, row_step);
-#pragma unroll
-        for (int u = 0; u < kSteps; ++u) step(L, w[u], vb + u * 32, true);
-      } else {
-#pragma unroll
-        for (int u = 0; u < kSteps; ++u) w[u] = vb + u * 32 < nfull ? buf[u * 32] : make_uint4(0, 0, 0, 0);
-        __syncwarp();
-        ++st.consumed;
-        produce_one(st, row_step);
-#pragma unroll
-        for (int u = 0; u < kSteps; ++u)
-          if (vb - lane + u * 32 < nfull) step(L, w[u], vb + u * 32, vb + u * 32 < nfull);  // warp-uniform
-      }
+      for (int u = 0; u < kWrLaneVecs; ++u) r[u] = lv[vu[u]];
+      const bool whole = c < nch - 1 || nfull % kWrChunkVecs == 0;  // warp-uniform
+      const uint32_t M = lane_mask(r, vu, whole ? kWrLaneVecs : nfull - v0, tval, tv2);
+      const char* lb = reinterpret_cast<const char*>(lv);
+      emit(M, v0 * VEC, &ccount, [&](int b) {
+        return ES == 2 ? static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(lb)[b])
+                       : reinterpret_cast<const uint32_t*>(lb)[b];
+      });
+      __syncwarp();  // every lane is done with the slot: refill it
+      ++st.consumed;
+      produce_one(st, row_step);
     }
-    if (nfull < p.nvec) {  // the ragged last vector
-      const bool in = lane == 0;
-      const uint4 w = in ? load_vec<ES>(rowp, nfull, p.len) : make_uint4(0, 0, 0, 0);
-      step(L, w, nfull, in);
-    }
-    *n = finish(L);
-    *nan = L.nan;
-    *kmax = __reduce_max_sync(kFull, L.kmax);
+    ragged(rowp, tval, tv2, &ccount);
+    *n = ccount;
     return true;
   }
   // Waits (bounded) for every copy still in flight.
@@ -540,12 +499,39 @@ struct WarpRow {
   }
 
   // ---- R + C on the candidates ---------------------------------------------------
-  // n candidates (k <= n <= cap), all with key >= tk, in index order.
-  // Returns the row's k-th key.
-  // kmax: the largest candidate key.
-  __device__ uint32_t select_candidates(int64_t row, int n, uint32_t tk, uint32_t kmax) const {
-    uint32_t lo = tk, hi = kmax, need = static_cast<uint32_t>(p.k);
-    for (;;) {
+  // n candidates (k <= n <= cap), every non-NaN one with key >= tk, in index
+  // order. Writes the row's top k and returns 1 with the k-th key in *kth, or
+  // returns 0 (nothing written) if a candidate is NaN.
+  __device__ int select_candidates(int64_t row, int n, uint32_t tk, uint32_t* kth_out) const {
+    constexpr int S0 = KB - 16;  // the first level bins the top 16 key bits
+    uint32_t need = static_cast<uint32_t>(p.k);
+    const uint32_t lo16 = tk >> S0;
+    wr_clear_hist(hist);
+    uint32_t over = 0;
+    bool nan = false;
+    for (int j = lane; j < n; j += 32) {
+      const uint32_t bits = bits_at(j);
+      nan |= is_nan_bits<ES>(bits);
+      const uint32_t d = (key_of<ES>(bits) >> S0) - lo16;
+      if (d < 256u) atomicAdd(&hist[d], 1u);
+      else ++over;
+    }
+    if (__any_sync(kFull, nan)) return 0;
+    over = __reduce_add_sync(kFull, over);
+    __syncwarp();
+    uint32_t lo, hi;
+    if (over < need) {  // the k-th key lies in the window
+      uint32_t above, cnt;
+      const uint32_t b = wr_find_bin(hist, need - over, &above, &cnt);
+      __syncwarp();
+      need -= over + above;
+      lo = (lo16 + b) << S0;
+      hi = lo + ((1u << S0) - 1u);
+    } else {  // above it (t far below the k-th key): the range up to the largest key
+      lo = (lo16 + 256u) << S0;
+      hi = KB == 16 ? 0xFFFFu : 0xFFFFFFFFu;
+    }
+    while (lo < hi) {  // 8-bit levels over [lo, hi]
       const uint32_t span = hi - lo;
       const int s = span < 256u ? 0 : (32 - __clz(span)) - 8;
       wr_clear_hist(hist);
@@ -590,7 +576,8 @@ struct WarpRow {
       }
       out += __popc(sb);
     }
-    return kth;
+    *kth_out = kth;
+    return 1;
   }
 
   // ---- exact k-th largest vector maximum (top 16 key bits) --------------------------
@@ -719,7 +706,6 @@ __global__ void __launch_bounds__(kWrThreads, 3) topk_warp_rows_kernel(const WrP
   const int warp = threadIdx.x >> 5;
   const WarpRow<ES> wr(p, smem + warp * wr_warp_bytes(ES, p.cap, p.depth));
   constexpr int KB = Traits<ES>::kKeyBits;
-  constexpr uint32_t kFull = 0xFFFFFFFFu;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWrWarps;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * kWrWarps + warp;
   if (wr.lane == 0) {
@@ -739,34 +725,31 @@ __global__ void __launch_bounds__(kWrThreads, 3) topk_warp_rows_kernel(const WrP
     const char* rowp = p.x + row * p.row_stride_bytes;
     uint32_t q = 0;
     uint32_t tk = have_guess ? guess : wr.sample_threshold(rowp, q = wr.default_rank());
-    bool nan = false;
     int n = 0;
-    uint32_t kmax = 0;
-    if (!wr.stream_pass(st, nwarps, rowp, tk, &n, &nan, &kmax)) {
+    if (!wr.stream_pass(st, nwarps, rowp, tk, &n)) {
       if (wr.lane == 0) atomicOr(p.flag, DS_TOPK_FLAG_TIMEOUT);
       wr.drain(st);
       return;
     }
-    bool bad = __any_sync(kFull, nan);
-    bool ok = !bad && n >= p.k && n <= p.cap;
+    // 1: selected; 0: a NaN among the candidates; -1: the guess did not hold
+    uint32_t kth = 0;
+    int status = (n >= p.k && n <= p.cap) ? wr.select_candidates(row, n, tk, &kth) : -1;
     // retries, each a direct pass over the row (from L2): the default sample
     // rank after a carried guess, then a rank adapted to the count just seen,
     // then the exact k-th largest vector maximum
-    for (int attempt = have_guess ? 0 : 1; !ok && !bad && attempt < 3; ++attempt) {
+    for (int attempt = have_guess ? 0 : 1; status < 0 && attempt < 3; ++attempt) {
       if (attempt == 0) q = wr.default_rank();
       if (attempt == 1) q = wr.adapted_rank(q, n);
       tk = attempt == 2 ? wr.vecmax_threshold(rowp) : wr.sample_threshold(rowp, q);
-      n = wr.direct_pass(rowp, tk, &nan, &kmax);
-      bad = __any_sync(kFull, nan);
-      ok = !bad && n >= p.k && n <= p.cap;
+      n = wr.direct_pass(rowp, tk);
+      if (n >= p.k && n <= p.cap) status = wr.select_candidates(row, n, tk, &kth);
     }
-    if (ok) {
-      const uint32_t kth = wr.select_candidates(row, n, tk, kmax);
+    if (status == 1) {
       const uint32_t m = (KB == 16 ? kWrGuessMargin : (kWrGuessMargin << 16));
       guess = kth > wr_key_floor<ES>() + m ? kth - m : wr_key_floor<ES>();
       have_guess = true;
     } else {
-      wr.exact_row(rowp, row);
+      wr.exact_row(rowp, row);  // also raises the NaN flag
     }
     __syncwarp();
   }
