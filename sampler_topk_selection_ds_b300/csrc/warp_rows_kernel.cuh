@@ -63,6 +63,7 @@ constexpr int kWrMaxDepth = 3;             // chunks in flight per warp
 #endif
 constexpr uint32_t kWrWaitLimit = DS_TOPK_WAIT_LIMIT;
 constexpr uint32_t kWrSuspendNs = 1000;      // a poll may sleep this long before it fails
+constexpr int kSelU = 4;                     // candidates per lane in flight in the selection passes
 
 static_assert(kWrLaneVecs == 4, "a lane's candidate mask holds 4 vectors of 8 bf16 elements");
 
@@ -509,12 +510,22 @@ struct WarpRow {
     wr_clear_hist(hist);
     uint32_t over = 0;
     bool nan = false;
-    for (int j = lane; j < n; j += 32) {
-      const uint32_t bits = bits_at(j);
-      nan |= is_nan_bits<ES>(bits);
-      const uint32_t d = (key_of<ES>(bits) >> S0) - lo16;
-      if (d < 256u) atomicAdd(&hist[d], 1u);
-      else ++over;
+    for (int j0 = 0; j0 < n; j0 += 32 * kSelU) {  // kSelU candidates per lane in flight
+      uint32_t bits[kSelU];
+#pragma unroll
+      for (int u = 0; u < kSelU; ++u) {
+        const int j = j0 + 32 * u + lane;
+        bits[u] = j < n ? bits_at(j) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kSelU; ++u) {
+        if (j0 + 32 * u + lane < n) {
+          nan |= is_nan_bits<ES>(bits[u]);
+          const uint32_t d = (key_of<ES>(bits[u]) >> S0) - lo16;
+          if (d < 256u) atomicAdd(&hist[d], 1u);
+          else ++over;
+        }
+      }
     }
     if (__any_sync(kFull, nan)) return 0;
     over = __reduce_add_sync(kFull, over);
@@ -553,28 +564,38 @@ struct WarpRow {
     // ordered output: ties (key == kth) are taken in index order, `need` of them
     int taken_eq = 0, out = 0;
     const int64_t obase = row * p.k;
-    for (int j0 = 0; j0 < n && out < p.k; j0 += 32) {
-      const int j = j0 + lane;
-      uint32_t bits = 0, key = 0;
-      if (j < n) {
-        bits = bits_at(j);
-        key = key_of<ES>(bits);
+    for (int j0 = 0; j0 < n && out < p.k; j0 += 32 * kSelU) {
+      uint32_t bits[kSelU], gtb[kSelU], eqb[kSelU];
+#pragma unroll
+      for (int u = 0; u < kSelU; ++u) {
+        const int j = j0 + 32 * u + lane;
+        bits[u] = j < n ? bits_at(j) : 0u;
       }
-      const bool eq = j < n && key == kth;
-      const uint32_t eqb = __ballot_sync(kFull, eq);
-      const bool sel = (j < n && key > kth) ||
-                       (eq && static_cast<uint32_t>(taken_eq + __popc(eqb & lt)) < need);
-      taken_eq += __popc(eqb);
-      const uint32_t sb = __ballot_sync(kFull, sel);
-      if (sel && out + __popc(sb & lt) < p.k) {
-        const int64_t o = obase + out + __popc(sb & lt);
-        put_index(p.out_indices, o, idx_at(j), p.idx64);
-        if (p.return_value) {
-          if constexpr (ES == 2) static_cast<uint16_t*>(p.out_values)[o] = static_cast<uint16_t>(bits);
-          else static_cast<uint32_t*>(p.out_values)[o] = bits;
+#pragma unroll
+      for (int u = 0; u < kSelU; ++u) {
+        const bool in = j0 + 32 * u + lane < n;
+        const uint32_t key = key_of<ES>(bits[u]);
+        gtb[u] = __ballot_sync(kFull, in && key > kth);
+        eqb[u] = __ballot_sync(kFull, in && key == kth);
+      }
+#pragma unroll
+      for (int u = 0; u < kSelU; ++u) {
+        // ties are taken in index order while fewer than `need` are taken
+        const bool eq = (eqb[u] >> lane) & 1u;
+        const bool sel = ((gtb[u] >> lane) & 1u) ||
+                         (eq && static_cast<uint32_t>(taken_eq + __popc(eqb[u] & lt)) < need);
+        taken_eq += __popc(eqb[u]);
+        const uint32_t sb = __ballot_sync(kFull, sel);
+        if (sel && out + __popc(sb & lt) < p.k) {
+          const int64_t o = obase + out + __popc(sb & lt);
+          put_index(p.out_indices, o, idx_at(j0 + 32 * u + lane), p.idx64);
+          if (p.return_value) {
+            if constexpr (ES == 2) static_cast<uint16_t*>(p.out_values)[o] = static_cast<uint16_t>(bits[u]);
+            else static_cast<uint32_t*>(p.out_values)[o] = bits[u];
+          }
         }
+        out += __popc(sb);
       }
-      out += __popc(sb);
     }
     *kth_out = kth;
     return 1;
