@@ -215,6 +215,16 @@ __device__ __forceinline__ int64_t get_index(const void* out, int64_t pos, int32
   return idx64 ? static_cast<const int64_t*>(out)[pos] : static_cast<int64_t>(static_cast<const int32_t*>(out)[pos]);
 }
 
+// Load a u16 from the same shared-memory offset in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_ld_u16(const uint16_t* local, uint32_t rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t ra;
+  uint16_t v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(ra) : "memory");
+  return v;
+}
+
 // Load a u32 from the same shared-memory offset in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t dsmem_ld_u32(const uint32_t* local, uint32_t rank) {
   const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
@@ -401,6 +411,7 @@ constexpr int kXpreGt = 6;    // [6]      cluster: selected '>' elements of lowe
 constexpr int kXpreEq = 7;    // [7]      cluster: '==' elements of lower ranks (pushed)
 constexpr int kOvw = 8;       // [8..11]  overflow words of cluster levels (local + 3 received)
 constexpr int kOvl = 12;      // [12]     overflow word of local levels
+constexpr int kRdTot = 13;    // [13]     fallback: listed granules of the whole row
 constexpr int kWtot = 16;     // [16..31] per-warp totals (2 x kWarps)
 constexpr int kSegBase = 32;  // [32..39] candidate segment start per warp
 constexpr int kSegCnt = 40;   // [40..47] candidate segment length per warp
@@ -625,6 +636,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     // exact mode: every granule's maximum key goes to M.
     // Both modes test every element for NaN through the NaN-propagating maxima.
     uint32_t t16 = 0;
+    uint32_t row_max16 = 0xFFFFFFFFu;  // the row's largest top-16 key, when the exact threshold found it
     int lc = 0;  // granules in this warp's list (warp-uniform)
     bool vec_kept = false;  // the list's vectors were copied to wvec by the streaming pass
     bool guess_mode = have_guess;
@@ -746,6 +758,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           cg::this_cluster().sync();
           mmax = misc[kXmax];
         }
+        row_max16 = mmax;
         const uint32_t wbase = mmax > 255u ? mmax - 255u : 0u;
         CL.begin();
         for (int b0 = sb; b0 < se; b0 += 256) {  // 8 maxima per lane per step
@@ -1142,23 +1155,90 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     } else if (!dense) {
       // ---- fallback: candidates did not fit; select over the listed granules, ------
       // re-read from global memory, with cluster-wide histograms.
+      //
+      // The listed granules of a row can sit in a few warps of one CTA (a sorted
+      // or ramp row lists only the top of the row). So they are first spread
+      // evenly over every warp of the cluster: the per-warp list counts of all
+      // CTAs give a prefix in (CTA, warp) order, which is index order, and
+      // global warp g takes the contiguous share [g T / G, (g + 1) T / G) of the
+      // concatenated lists, read from the owners' shared memory into its own
+      // (the granule maxima and candidate arrays are dead here).
+      const int G = kWarps * S;
+      uint32_t* gcnt = misc + kAll;      // [G] listed granules per (CTA, warp)
+      uint32_t* gpre = misc + kAll + G;  // [G] their exclusive prefix
+      __syncthreads();                   // the published counts in misc[kAll..] are read
+      if (tid < G) {
+        if constexpr (S > 1) gcnt[tid] = dsmem_ld_u32(misc + kLcnt + tid % kWarps, static_cast<uint32_t>(tid / kWarps));
+        else gcnt[tid] = misc[kLcnt + tid];
+      }
+      __syncthreads();
+      if (warp == 0) {
+        uint32_t c[4], sum = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int q = lane * 4 + i;
+          c[i] = q < G ? gcnt[q] : 0u;
+          sum += c[i];
+        }
+        uint32_t run = warp_excl_scan(sum);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int q = lane * 4 + i;
+          if (q < G) gpre[q] = run;
+          run += c[i];
+        }
+        if (lane == 31) misc[kRdTot] = run;
+      }
+      __syncthreads();
+      const uint32_t rd_total = misc[kRdTot];
+      const int rd_cap = static_cast<int>(union_bytes(p.g_cap_pad, p.cand_cap) / 4 / kWarps);
+      const bool rd = gv == 1 && G > 1 && (rd_total + G - 1) / G <= static_cast<uint32_t>(rd_cap);  // cluster-uniform
+      uint32_t* ra = reinterpret_cast<uint32_t*>(uni) + warp * rd_cap;  // this warp's share: row vector indices
+      int rn = 0;
+      if (rd) {
+        const uint32_t g = static_cast<uint32_t>(rank * kWarps + warp);
+        const uint32_t a = static_cast<uint32_t>(static_cast<uint64_t>(g) * rd_total / G);
+        const uint32_t b = static_cast<uint32_t>(static_cast<uint64_t>(g + 1) * rd_total / G);
+        rn = static_cast<int>(b - a);
+        for (uint32_t j = a + lane; j < b; j += 32) {
+          int lo = 0, hi = G - 1;  // the last (CTA, warp) whose list starts at or before j
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (gpre[mid] <= j) lo = mid;
+            else hi = mid - 1;
+          }
+          const int orank = lo / kWarps, ow = lo % kWarps;
+          const int64_t onv = min(p.vec_per_cta, p.nvec - orank * p.vec_per_cta);  // vectors of its slice
+          const int osegm = round_up32(static_cast<int>((onv + kWarps - 1) / kWarps));
+          const uint16_t* ol = list + ow * osegm + (j - gpre[lo]);
+          uint32_t e;
+          if constexpr (S > 1) e = dsmem_ld_u16(ol, static_cast<uint32_t>(orank));
+          else e = *ol;
+          ra[j - a] = static_cast<uint32_t>(orank * p.vec_per_cta) + e;
+        }
+        __syncwarp();
+      }
+      const int lcnt = rd ? rn : lc;  // this warp's listed granules, after spreading
+      auto vec_at = [&](int j) -> int {  // row vector index of the warp's j-th listed granule
+        return rd ? static_cast<int>(ra[j]) : static_cast<int>(v0) + static_cast<int>(wlist[j]);
+      };
       auto visit = [&](auto&& f) {
         if (gv == 1) {  // 4 listed vectors in flight per lane (row vector indices fit 32 bits)
           constexpr int UV = 4;
-          const int iv0 = static_cast<int>(v0), iv1 = static_cast<int>(v1), ilen = static_cast<int>(p.len);
-          for (int jb = 0; jb < lc; jb += 32 * UV) {
+          const int ilen = static_cast<int>(p.len);
+          for (int jb = 0; jb < lcnt; jb += 32 * UV) {
             uint4 w[UV];
             int v[UV];
 #pragma unroll
             for (int u = 0; u < UV; ++u) {
               const int j = jb + 32 * u + lane;
-              v[u] = j < lc ? iv0 + static_cast<int>(wlist[j]) : iv1;
+              v[u] = j < lcnt ? vec_at(j) : -1;
               w[u] = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
-              if (v[u] < iv1) w[u] = load_vec<ES>(rowp, v[u], p.len);
+              if (v[u] >= 0) w[u] = load_vec<ES>(rowp, v[u], p.len);
             }
 #pragma unroll
             for (int u = 0; u < UV; ++u) {
-              const bool vok = v[u] < iv1;
+              const bool vok = v[u] >= 0;
 #pragma unroll
               for (int e = 0; e < VEC; ++e) {
                 const uint32_t eb = elem_bits<ES>(w[u], e);
@@ -1186,61 +1266,68 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         }
       };
       uint32_t need = k, kstar = 0;
-      {
-        // the 256 top-16 key values from t16 up, with a count of the keys above
-        const uint32_t wbase = t16;
-        CL.begin();
-        uint32_t* h = CL.loc();
-        uint32_t lover = 0;
-        visit([&](uint32_t key, bool ok) {
-          const uint32_t k16v = key >> (KB - 16);
-          ok = ok && k16v >= wbase;
-          const uint32_t d = k16v - wbase;
-          hist_add(h, d, ok && d < 256u);
-          lover += __popc(__ballot_sync(kFull, ok && d >= 256u));
-        });
-        if (lane == 0 && lover) atomicAdd(CL.ov(), lover);
-        const LevelResult r = CL.finish<S>(lvl++, need);
-        if (r.shift && wbase + 256u <= 0xFFFFu) {
-          // the k-th key lies above the window (t far below it, e.g. when k exceeds
-          // the number of granules with a finite maximum): two 8-bit levels over
-          // the top 16 key bits of the keys above the window
-          const uint32_t lo16 = wbase + 256u;
-          CL.begin();
-          h = CL.loc();
-          visit([&](uint32_t key, bool ok) {
-            const uint32_t k16v = key >> (KB - 16);
-            hist_add(h, k16v >> 8, ok && k16v >= lo16);
-          });
-          const LevelResult ra = CL.finish<S>(lvl++, need);
-          need -= ra.above;
-          CL.begin();
-          h = CL.loc();
-          visit([&](uint32_t key, bool ok) {
-            const uint32_t k16v = key >> (KB - 16);
-            hist_add(h, k16v & 0xFFu, ok && k16v >= lo16 && (k16v >> 8) == ra.digit);
-          });
-          const LevelResult rb = CL.finish<S>(lvl++, need);
-          need -= rb.above;
-          kstar = ((ra.digit << 8) | rb.digit) << (KB - 16);
-        } else {
-          kstar = (wbase + r.digit) << (KB - 16);
-          need -= r.above;
-        }
-      }
-      if constexpr (KB == 32) {
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-          const int shift = 8 - 8 * j;
+      if (KB == 16 && row_max16 == t16) {
+        // at least k granule maxima equal the row's largest key, so at least k
+        // elements do: that key is the k-th key, and the lowest-index k of the
+        // elements holding it are the row's top k (rows of a few repeated levels)
+        kstar = t16;
+      } else {
+        {
+          // the 256 top-16 key values from t16 up, with a count of the keys above
+          const uint32_t wbase = t16;
           CL.begin();
           uint32_t* h = CL.loc();
-          const uint32_t pre = kstar >> (shift + 8);
+          uint32_t lover = 0;
           visit([&](uint32_t key, bool ok) {
-            hist_add(h, (key >> shift) & 0xFFu, ok && (key >> (shift + 8)) == pre);
+            const uint32_t k16v = key >> (KB - 16);
+            ok = ok && k16v >= wbase;
+            const uint32_t d = k16v - wbase;
+            hist_add(h, d, ok && d < 256u);
+            lover += __popc(__ballot_sync(kFull, ok && d >= 256u));
           });
+          if (lane == 0 && lover) atomicAdd(CL.ov(), lover);
           const LevelResult r = CL.finish<S>(lvl++, need);
-          kstar |= r.digit << shift;
-          need -= r.above;
+          if (r.shift && wbase + 256u <= 0xFFFFu) {
+            // the k-th key lies above the window (t far below it, e.g. when k exceeds
+            // the number of granules with a finite maximum): two 8-bit levels over
+            // the top 16 key bits of the keys above the window
+            const uint32_t lo16 = wbase + 256u;
+            CL.begin();
+            h = CL.loc();
+            visit([&](uint32_t key, bool ok) {
+              const uint32_t k16v = key >> (KB - 16);
+              hist_add(h, k16v >> 8, ok && k16v >= lo16);
+            });
+            const LevelResult ra = CL.finish<S>(lvl++, need);
+            need -= ra.above;
+            CL.begin();
+            h = CL.loc();
+            visit([&](uint32_t key, bool ok) {
+              const uint32_t k16v = key >> (KB - 16);
+              hist_add(h, k16v & 0xFFu, ok && k16v >= lo16 && (k16v >> 8) == ra.digit);
+            });
+            const LevelResult rb = CL.finish<S>(lvl++, need);
+            need -= rb.above;
+            kstar = ((ra.digit << 8) | rb.digit) << (KB - 16);
+          } else {
+            kstar = (wbase + r.digit) << (KB - 16);
+            need -= r.above;
+          }
+        }
+        if constexpr (KB == 32) {
+  #pragma unroll 1
+          for (int j = 0; j < 2; ++j) {
+            const int shift = 8 - 8 * j;
+            CL.begin();
+            uint32_t* h = CL.loc();
+            const uint32_t pre = kstar >> (shift + 8);
+            visit([&](uint32_t key, bool ok) {
+              hist_add(h, (key >> shift) & 0xFFu, ok && (key >> (shift + 8)) == pre);
+            });
+            const LevelResult r = CL.finish<S>(lvl++, need);
+            kstar |= r.digit << shift;
+            need -= r.above;
+          }
         }
       }
       const uint32_t r_ties = need;
@@ -1320,18 +1407,18 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         // 4 listed vectors in flight per lane, handled in list order; stop once
         // every later output would land at or beyond position k
         constexpr int UV = 4;
-        for (int jb = 0; jb < (none_here ? 0 : lc); jb += 32 * UV) {
+        for (int jb = 0; jb < (none_here ? 0 : lcnt); jb += 32 * UV) {
           uint4 w[UV];
           int64_t v[UV];
 #pragma unroll
           for (int u = 0; u < UV; ++u) {
             const int j = jb + 32 * u + lane;
-            v[u] = j < lc ? v0 + static_cast<int64_t>(wlist[j]) : v1;
+            v[u] = j < lcnt ? static_cast<int64_t>(vec_at(j)) : -1;
             w[u] = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
-            if (v[u] < v1) w[u] = load_vec<ES>(rowp, v[u], p.len);
+            if (v[u] >= 0) w[u] = load_vec<ES>(rowp, v[u], p.len);
           }
 #pragma unroll
-          for (int u = 0; u < UV; ++u) write_vec(w[u], v[u], v[u] < v1);
+          for (int u = 0; u < UV; ++u) write_vec(w[u], v[u], v[u] >= 0);
           if (base_gt + min(base_eq, r_ties) >= k) break;
         }
       } else {
