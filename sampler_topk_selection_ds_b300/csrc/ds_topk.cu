@@ -87,43 +87,10 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
   out->warp_rows = false;
   out->unaligned = false;
 
-  // Rows that do not all start on a 16-byte boundary: one CTA per row, radix
-  // selection over the aligned vectors that overlap the row.
-  if (!x_aligned || (row_stride * es) % 16 != 0) {
-    out->es = es;
-    out->unaligned = true;
-    ds_topk_plan_t& pl = out->pub;
-    pl.path = DS_TOPK_PATH_UNALIGNED;
-    pl.cluster_size = 1;
-    pl.threads_per_cta = ds_topk_dev::kUaThreads;
-    pl.vectors_per_granule = 1;
-    // candidate keys of a guessed threshold (about 1.5 k expected; also holds
-    // the first-row sample)
-    int64_t cap = 4 * static_cast<int64_t>(k) + 2048;
-    if (cap < ds_topk_dev::kUaSampleKeys) cap = ds_topk_dev::kUaSampleKeys;
-    // persistent: each CTA walks rows with a stride of the grid, so the grid may
-    // be capped at the largest launchable size
-    pl.grid_ctas = batch < INT32_MAX ? batch : INT32_MAX;
-    pl.granules_per_cta = cap;
-    pl.smem_bytes = static_cast<int32_t>(cap * 4);
-    pl.launches = batch > 0 ? 1 : 0;
-    ds_topk_dev::UaParams& u = out->uprm;
-    u.x = nullptr;
-    u.batch = batch;
-    u.row_stride_bytes = row_stride * es;
-    u.len = len;
-    u.k = k;
-    u.cap = static_cast<int32_t>(cap);
-    u.return_value = 0;
-    u.out_values = nullptr;
-    u.out_indices = nullptr;
-    u.idx64 = 0;
-    u.flag = nullptr;
-    return DS_TOPK_OK;
-  }
-
   // Many short rows: one warp per row (candidate indices fit 16 bits, and a
   // warp's candidate buffer of about 2k entries leaves room for 2+ CTAs per SM).
+  // Rows need not start on a 16-byte boundary: the kernel reads the 16-byte
+  // blocks that overlap each row and masks the elements outside it.
   if (len <= ds_topk_dev::kWrMaxLen && k <= ds_topk_dev::kWrMaxK &&
       batch >= wr_min_rows_per_sm(len) * static_cast<int64_t>(sm_count)) {
     int64_t cap = 2 * static_cast<int64_t>(k) + 256;
@@ -165,7 +132,6 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
       w.batch = batch;
       w.row_stride_bytes = row_stride * es;
       w.len = static_cast<int32_t>(len);
-      w.nvec = static_cast<int32_t>(nvec);
       w.cap = static_cast<int32_t>(cap);
       w.depth = depth;
       w.k = k;
@@ -176,6 +142,41 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
       w.flag = nullptr;
       return DS_TOPK_OK;
     }
+  }
+
+  // Rows that do not all start on a 16-byte boundary: one CTA per row, radix
+  // selection over the aligned vectors that overlap the row.
+  if (!x_aligned || (row_stride * es) % 16 != 0) {
+    out->es = es;
+    out->unaligned = true;
+    ds_topk_plan_t& pl = out->pub;
+    pl.path = DS_TOPK_PATH_UNALIGNED;
+    pl.cluster_size = 1;
+    pl.threads_per_cta = ds_topk_dev::kUaThreads;
+    pl.vectors_per_granule = 1;
+    // candidate keys of a guessed threshold (about 1.5 k expected; also holds
+    // the first-row sample)
+    int64_t cap = 4 * static_cast<int64_t>(k) + 2048;
+    if (cap < ds_topk_dev::kUaSampleKeys) cap = ds_topk_dev::kUaSampleKeys;
+    // persistent: each CTA walks rows with a stride of the grid, so the grid may
+    // be capped at the largest launchable size
+    pl.grid_ctas = batch < INT32_MAX ? batch : INT32_MAX;
+    pl.granules_per_cta = cap;
+    pl.smem_bytes = static_cast<int32_t>(cap * 4);
+    pl.launches = batch > 0 ? 1 : 0;
+    ds_topk_dev::UaParams& u = out->uprm;
+    u.x = nullptr;
+    u.batch = batch;
+    u.row_stride_bytes = row_stride * es;
+    u.len = len;
+    u.k = k;
+    u.cap = static_cast<int32_t>(cap);
+    u.return_value = 0;
+    u.out_values = nullptr;
+    u.out_indices = nullptr;
+    u.idx64 = 0;
+    u.flag = nullptr;
+    return DS_TOPK_OK;
   }
 
   int S = 1;

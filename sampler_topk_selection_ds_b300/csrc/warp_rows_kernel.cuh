@@ -72,7 +72,6 @@ struct WrParams {
   int64_t batch;
   int64_t row_stride_bytes;
   int32_t len;
-  int32_t nvec;           // ceil(len / VEC)
   int32_t cap;            // candidate slots per warp (multiple of 32)
   int32_t depth;          // chunks of the streaming ring (2 or 3)
   int32_t k;
@@ -238,8 +237,6 @@ struct WarpRow {
   int lane;
   uint32_t lt;
   int rot;        // rotation of the lane's four loads (conflict-free shared-memory reads)
-  int nfull;      // vectors wholly inside a row
-  int nch;        // bulk chunks per row (they cover the nfull whole vectors)
 
   __device__ WarpRow(const WrParams& prm, unsigned char* base)
       : p(prm),
@@ -250,13 +247,62 @@ struct WarpRow {
         ci(reinterpret_cast<uint16_t*>(base + prm.depth * kWrChunk + kWrFixedBytes) + 2 * prm.cap),
         lane(threadIdx.x & 31),
         lt(lanemask_lt()),
-        rot((threadIdx.x >> 1) & 3),
-        nfull(prm.len / VEC),
-        nch((prm.len / VEC + kWrChunkVecs - 1) / kWrChunkVecs) {}
+        rot((threadIdx.x >> 1) & 3) {}
 
-  __device__ __forceinline__ uint4 load(const char* rowp, int v) const {
-    if ((v + 1) * VEC <= p.len) return ld_nc_v4(rowp + static_cast<int64_t>(v) * 16);
-    return load_vec<ES>(rowp, v, p.len);
+  // ---- where a row lies: the 16-byte blocks that overlap it ---------------------
+  // A row may start anywhere on its element size. It is read as the 16-byte
+  // aligned blocks that overlap [0, len): block v holds row elements
+  // v*VEC + e - lead for e = 0..VEC-1. Elements outside [0, len) that share a
+  // block with row elements are masked before anything looks at them; no block
+  // without a row element is read (and an aligned 16-byte block never crosses a
+  // page, so the reads stay inside the row's pages).
+  struct Geo {
+    const char* base;  // the first block
+    int lead;          // elements of the first block before the row's element 0
+    int nv;            // blocks overlapping the row
+    int nch;           // bulk chunks covering them
+  };
+  __device__ __forceinline__ Geo geo(int64_t row) const {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p.x + row * p.row_stride_bytes);
+    Geo g;
+    g.base = reinterpret_cast<const char*>(a & ~static_cast<uintptr_t>(15));
+    g.lead = static_cast<int>((a & 15u) / ES);
+    g.nv = (g.lead + p.len + VEC - 1) / VEC;
+    g.nch = (g.nv + kWrChunkVecs - 1) / kWrChunkVecs;
+    return g;
+  }
+  // Block v with every element outside the row set to -inf (only the first and
+  // the last block can hold such elements).
+  __device__ __forceinline__ uint4 load(const Geo& g, int v) const {
+    uint4 w = ld_nc_v4(g.base + static_cast<int64_t>(v) * 16);
+    if (v == 0 || v == g.nv - 1) {
+      uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const int idx = v * VEC + e - g.lead;
+        if (idx < 0 || idx >= p.len) {
+          if constexpr (ES == 2) {
+            const int sh = (e & 1) * 16;
+            ws[e >> 1] = (ws[e >> 1] & ~(0xFFFFu << sh)) | (0xFF80u << sh);
+          } else {
+            ws[e] = 0xFF800000u;
+          }
+        }
+      }
+      w = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+    }
+    return w;
+  }
+  // Mask of the row elements among a lane's 4 blocks v0 .. v0+3 (bit VEC*u + e
+  // for element e of block v0 + u).
+  __device__ __forceinline__ uint32_t valid_bits(const Geo& g, int v0) const {
+    constexpr int W = kWrLaneVecs * VEC;
+    const int lo = g.lead - v0 * VEC;  // bit of row element 0
+    const int a = lo > 0 ? lo : 0;
+    const int b = lo + p.len < W ? lo + p.len : W;
+    if (b <= a) return 0u;
+    const uint32_t upto = b >= 32 ? 0xFFFFFFFFu : ((1u << b) - 1u);
+    return upto & ~((1u << a) - 1u);
   }
 
   // Top 16 bits of the key of a packed maximum (bf16: the key itself).
@@ -272,13 +318,13 @@ struct WarpRow {
   // 1/8 of a 64 KB row's cache lines, which the stream then finds in L2), and the
   // threshold is the q-th largest sampled maximum, q about 1.2 k times the
   // sampled fraction plus a margin: a guess that the stream verifies.
-  __device__ __forceinline__ int sample_size() const {
-    return p.nvec <= 32 * kWrSampleBlocks ? p.nvec : 32 * kWrSampleBlocks;
+  __device__ __forceinline__ int sample_size(const Geo& g) const {
+    return g.nv <= 32 * kWrSampleBlocks ? g.nv : 32 * kWrSampleBlocks;
   }
   // The rank q of the sampled maximum used as the first-row threshold.
-  __device__ __forceinline__ uint32_t default_rank() const {
-    if (p.nvec <= 32 * kWrSampleBlocks) return static_cast<uint32_t>(p.k);
-    return static_cast<uint32_t>((static_cast<int64_t>(6 * p.k) * sample_size() / 5 + p.nvec - 1) / p.nvec + 8);
+  __device__ __forceinline__ uint32_t default_rank(const Geo& g) const {
+    if (g.nv <= 32 * kWrSampleBlocks) return static_cast<uint32_t>(p.k);
+    return static_cast<uint32_t>((static_cast<int64_t>(6 * p.k) * sample_size(g) / 5 + g.nv - 1) / g.nv + 8);
   }
   // A rank for a second try after the threshold of rank q gave n candidates:
   // candidates grow about in proportion to q.
@@ -288,8 +334,8 @@ struct WarpRow {
     else r = static_cast<uint32_t>(static_cast<int64_t>(q) * (5 * p.k / 4) / (n > 0 ? n : 1)) + 4;
     return r < 1u ? 1u : r;
   }
-  __device__ uint32_t sample_threshold(const char* rowp, uint32_t q) const {
-    const int nvec = p.nvec;
+  __device__ uint32_t sample_threshold(const Geo& g, uint32_t q) const {
+    const int nvec = g.nv;
     constexpr int kPer = kWrSampleBlocks;  // vectors per lane
     const bool whole = nvec <= 32 * kPer;
     const int ns = whole ? nvec : 32 * kPer;
@@ -299,7 +345,7 @@ struct WarpRow {
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int v = i * bstride + lane;
-      kk[i] = (whole ? v < nvec : true) ? key16(vec_max<ES>(load(rowp, v))) : 0xFFFFFFFFu;
+      kk[i] = (whole ? v < nvec : true) ? key16(vec_max<ES>(load(g, v))) : 0xFFFFFFFFu;
     }
     wr_clear_hist(hist);
 #pragma unroll
@@ -380,70 +426,65 @@ struct WarpRow {
   }
 
   // The retry pass: the row straight from global memory (it was just streamed,
-  // so mostly from L2), 4 consecutive vectors per lane. Returns the candidate
+  // so mostly from L2), 4 consecutive blocks per lane. Returns the candidate
   // count (it may exceed cap; writes stop there).
-  __device__ int direct_pass(const char* rowp, uint32_t tk) const {
+  __device__ int direct_pass(const Geo& g, uint32_t tk) const {
     const float tval = key_threshold_value<ES>(tk);
     const uint32_t tv2 = (__float_as_uint(tval) >> 16) * 0x00010001u;
     const int vu[kWrLaneVecs] = {0, 1, 2, 3};
     int ccount = 0;
-    for (int g = 0; g < nfull; g += kWrChunkVecs) {
-      const int v0 = g + lane * kWrLaneVecs;
+    for (int c0 = 0; c0 < g.nv; c0 += kWrChunkVecs) {
+      const int v0 = c0 + lane * kWrLaneVecs;
       uint4 r[kWrLaneVecs];
 #pragma unroll
       for (int u = 0; u < kWrLaneVecs; ++u)
-        r[u] = v0 + u < nfull ? ld_nc_v4(rowp + static_cast<int64_t>(v0 + u) * 16) : make_uint4(0, 0, 0, 0);
-      const uint32_t M = lane_mask(r, vu, nfull - v0, tval, tv2);
-      emit(M, v0 * VEC, &ccount, [&](int b) { return reg_bits(r, b); });
+        r[u] = v0 + u < g.nv ? ld_nc_v4(g.base + static_cast<int64_t>(v0 + u) * 16) : make_uint4(0, 0, 0, 0);
+      uint32_t M = lane_mask(r, vu, g.nv - v0, tval, tv2);
+      if (c0 == 0 || c0 + kWrChunkVecs >= g.nv) M &= valid_bits(g, v0);  // warp-uniform
+      emit(M, v0 * VEC - g.lead, &ccount, [&](int b) { return reg_bits(r, b); });
     }
-    ragged(rowp, tval, tv2, &ccount);
     return ccount;
-  }
-
-  // The ragged last vector of a row (len not a multiple of VEC): scalar loads,
-  // elements at or past len masked off; its candidates come last in index order.
-  __device__ __forceinline__ void ragged(const char* rowp, float tval, uint32_t tv2, int* ccount) const {
-    if (nfull == p.nvec) return;  // warp-uniform
-    uint4 w = make_uint4(0, 0, 0, 0);
-    uint32_t m = 0;
-    if (lane == 0) {
-      w = load_vec<ES>(rowp, nfull, p.len);
-      m = vec_cand_bits<ES>(w, tval, tv2) & ((1u << (p.len - nfull * VEC)) - 1u);
-    }
-    emit(m, nfull * VEC, ccount, [&](int b) { return elem_bits<ES>(w, b); });
   }
 
   // ---- the streaming ring: chunks of the warp's rows, in order, depth ahead -------
   struct Stream {
     const char* src;    // source of the next chunk to copy (null: none left)
     int64_t prow;       // its row
-    int pchunk;         // its chunk index in that row
+    int pleft;          // chunks of that row still to copy, src's included
+    uint32_t plast;     // bytes of that row's last chunk
     int pslot;          // ring slot it goes to
     int cslot;          // ring slot of the next chunk to read
     uint32_t cphase;    // mbarrier phase parity that chunk completes
     uint32_t issued;    // chunks copied so far
     uint32_t consumed;  // chunks read so far
   };
+  // Points the producer at row `row` (or at nothing past the batch).
+  __device__ __forceinline__ void stream_row(Stream& st, int64_t row) const {
+    st.prow = row;
+    if (row < p.batch) {
+      const Geo g = geo(row);
+      st.src = g.base;
+      st.pleft = g.nch;
+      st.plast = static_cast<uint32_t>(g.nv - (g.nch - 1) * kWrChunkVecs) * 16u;
+    } else {
+      st.src = nullptr;
+    }
+  }
   __device__ __forceinline__ void stream_begin(Stream& st, int64_t first) const {
-    st.prow = first;
-    st.src = (first < p.batch && nch > 0) ? p.x + first * p.row_stride_bytes : nullptr;
-    st.pchunk = st.pslot = st.cslot = 0;
+    stream_row(st, first);
+    st.pslot = st.cslot = 0;
     st.cphase = st.issued = st.consumed = 0u;
   }
   // Copies the next chunk of the warp's row sequence into the ring, if any.
   __device__ __forceinline__ void produce_one(Stream& st, int64_t row_step) const {
     if (st.src == nullptr) return;
-    const bool last = st.pchunk == nch - 1;
-    const uint32_t bytes = last ? static_cast<uint32_t>(nfull * 16 - (nch - 1) * kWrChunk) : kWrChunk;
+    const uint32_t bytes = st.pleft == 1 ? st.plast : static_cast<uint32_t>(kWrChunk);
     if (lane == 0) bulk_load(chunks + st.pslot * kWrChunkVecs, st.src, bytes, mbar + st.pslot);
     if (++st.pslot == p.depth) st.pslot = 0;
     ++st.issued;
-    if (last) {
-      st.pchunk = 0;
-      st.prow += row_step;
-      st.src = st.prow < p.batch ? p.x + st.prow * p.row_stride_bytes : nullptr;
+    if (--st.pleft == 0) {
+      stream_row(st, st.prow + row_step);
     } else {
-      ++st.pchunk;
       st.src += kWrChunk;
     }
   }
@@ -451,31 +492,33 @@ struct WarpRow {
   // with the chunk `depth` places further on once its candidates are copied out.
   // Returns false if a copy never completed within the poll limit (the warp must
   // then stop); else the candidate count in *n (it may exceed cap).
-  __device__ bool stream_pass(Stream& st, int64_t row_step, const char* rowp, uint32_t tk, int* n) const {
+  __device__ bool stream_pass(Stream& st, int64_t row_step, const Geo& g, uint32_t tk, int* n) const {
     const float tval = key_threshold_value<ES>(tk);
     const uint32_t tv2 = (__float_as_uint(tval) >> 16) * 0x00010001u;
     int vu[kWrLaneVecs];
 #pragma unroll
     for (int u = 0; u < kWrLaneVecs; ++u) vu[u] = (u + rot) & (kWrLaneVecs - 1);
     int ccount = 0;
-    for (int c = 0; c < nch; ++c) {
+    for (int c = 0; c < g.nch; ++c) {
       const int slot = st.cslot;
       if (!__all_sync(kFull, mbar_wait(mbar + slot, st.cphase))) return false;
       if (++st.cslot == p.depth) {
         st.cslot = 0;
         st.cphase ^= 1u;
       }
-      // the lane's 64 bytes; load u reads vector vu[u], so the 8 lanes of each
+      // the lane's 64 bytes; load u reads block vu[u], so the 8 lanes of each
       // quarter-warp touch 8 distinct 16-byte bank groups
       const uint4* lv = chunks + slot * kWrChunkVecs + lane * kWrLaneVecs;
       const int v0 = c * kWrChunkVecs + lane * kWrLaneVecs;
       uint4 r[kWrLaneVecs];
 #pragma unroll
       for (int u = 0; u < kWrLaneVecs; ++u) r[u] = lv[vu[u]];
-      const bool whole = c < nch - 1 || nfull % kWrChunkVecs == 0;  // warp-uniform
-      const uint32_t M = lane_mask(r, vu, whole ? kWrLaneVecs : nfull - v0, tval, tv2);
+      uint32_t M = lane_mask(r, vu, kWrLaneVecs, tval, tv2);
+      // the first and the last chunk hold elements outside the row (and stale
+      // blocks past the row's last one): only row elements count
+      if (c == 0 || c == g.nch - 1) M &= valid_bits(g, v0);  // warp-uniform
       const char* lb = reinterpret_cast<const char*>(lv);
-      emit(M, v0 * VEC, &ccount, [&](int b) {
+      emit(M, v0 * VEC - g.lead, &ccount, [&](int b) {
         return ES == 2 ? static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(lb)[b])
                        : reinterpret_cast<const uint32_t*>(lb)[b];
       });
@@ -483,7 +526,6 @@ struct WarpRow {
       ++st.consumed;
       produce_one(st, row_step);
     }
-    ragged(rowp, tval, tv2, &ccount);
     *n = ccount;
     return true;
   }
@@ -604,16 +646,16 @@ struct WarpRow {
   // ---- exact k-th largest vector maximum (top 16 key bits) --------------------------
   // Two passes over the row, one histogram update per vector. At least k
   // elements reach the result, so it is a threshold that always holds.
-  __device__ uint32_t vecmax_threshold(const char* rowp) const {
-    if (p.nvec < p.k) return wr_key_floor<ES>();
-    const int nsteps = (p.nvec + 31) / 32;
+  __device__ uint32_t vecmax_threshold(const Geo& g) const {
+    if (g.nv < p.k) return wr_key_floor<ES>();
+    const int nsteps = (g.nv + 31) / 32;
     uint32_t need = static_cast<uint32_t>(p.k), b1 = 0;
     for (int level = 0; level < 2; ++level) {
       wr_clear_hist(hist);
       for (int i = 0; i < nsteps; ++i) {
         const int v = i * 32 + lane;
-        if (v < p.nvec) {
-          const uint32_t kk = key16(vec_max<ES>(load(rowp, v)));
+        if (v < g.nv) {
+          const uint32_t kk = key16(vec_max<ES>(load(g, v)));
           if (level == 0) atomicAdd(&hist[kk >> 8], 1u);
           else if ((kk >> 8) == b1) atomicAdd(&hist[kk & 0xFFu], 1u);
         }
@@ -632,8 +674,8 @@ struct WarpRow {
   }
 
   // ---- exact fallback: radix levels over every element, then an ordered pass ------
-  __device__ void exact_row(const char* rowp, int64_t row) const {
-    const int nvec = p.nvec;
+  __device__ void exact_row(const Geo& g, int64_t row) const {
+    const int nvec = g.nv;
     const int nsteps = (nvec + 31) / 32;
     uint32_t prefix = 0, need = static_cast<uint32_t>(p.k);
     bool nan = false;
@@ -643,10 +685,11 @@ struct WarpRow {
       for (int i = 0; i < nsteps; ++i) {
         const int v = i * 32 + lane;
         if (v >= nvec) continue;
-        const uint4 w = load(rowp, v);
+        const uint4 w = load(g, v);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-          if (v * VEC + e < p.len) {
+          const int idx = v * VEC + e - g.lead;
+          if (idx >= 0 && idx < p.len) {
             const uint32_t bits = elem_bits<ES>(w, e);
             if (done == 0) nan |= is_nan_bits<ES>(bits);
             const uint32_t key = key_of<ES>(bits);
@@ -670,10 +713,11 @@ struct WarpRow {
       uint4 w = make_uint4(0, 0, 0, 0);
       uint32_t mgt = 0, meq = 0;
       if (v < nvec) {
-        w = load(rowp, v);
+        w = load(g, v);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-          if (v * VEC + e < p.len) {
+          const int idx = v * VEC + e - g.lead;
+          if (idx >= 0 && idx < p.len) {
             const uint32_t key = key_of<ES>(elem_bits<ES>(w, e));
             mgt |= static_cast<uint32_t>(key > kth) << e;
             meq |= static_cast<uint32_t>(key == kth) << e;
@@ -701,7 +745,7 @@ struct WarpRow {
       while (msel && o < obase + p.k) {
         const int e = __ffs(msel) - 1;
         msel &= msel - 1;
-        put_index(p.out_indices, o, v * VEC + e, p.idx64);
+        put_index(p.out_indices, o, v * VEC + e - g.lead, p.idx64);
         if (p.return_value) {
           const uint32_t bits = elem_bits<ES>(w, e);
           if constexpr (ES == 2) static_cast<uint16_t*>(p.out_values)[o] = static_cast<uint16_t>(bits);
@@ -743,11 +787,11 @@ __global__ void __launch_bounds__(kWrThreads, 3) topk_warp_rows_kernel(const WrP
   bool have_guess = false;
   uint32_t guess = 0;
   for (int64_t row = first; row < p.batch; row += nwarps) {
-    const char* rowp = p.x + row * p.row_stride_bytes;
+    const typename WarpRow<ES>::Geo g = wr.geo(row);
     uint32_t q = 0;
-    uint32_t tk = have_guess ? guess : wr.sample_threshold(rowp, q = wr.default_rank());
+    uint32_t tk = have_guess ? guess : wr.sample_threshold(g, q = wr.default_rank(g));
     int n = 0;
-    if (!wr.stream_pass(st, nwarps, rowp, tk, &n)) {
+    if (!wr.stream_pass(st, nwarps, g, tk, &n)) {
       if (wr.lane == 0) atomicOr(p.flag, DS_TOPK_FLAG_TIMEOUT);
       wr.drain(st);
       return;
@@ -759,10 +803,10 @@ __global__ void __launch_bounds__(kWrThreads, 3) topk_warp_rows_kernel(const WrP
     // rank after a carried guess, then a rank adapted to the count just seen,
     // then the exact k-th largest vector maximum
     for (int attempt = have_guess ? 0 : 1; status < 0 && attempt < 3; ++attempt) {
-      if (attempt == 0) q = wr.default_rank();
+      if (attempt == 0) q = wr.default_rank(g);
       if (attempt == 1) q = wr.adapted_rank(q, n);
-      tk = attempt == 2 ? wr.vecmax_threshold(rowp) : wr.sample_threshold(rowp, q);
-      n = wr.direct_pass(rowp, tk);
+      tk = attempt == 2 ? wr.vecmax_threshold(g) : wr.sample_threshold(g, q);
+      n = wr.direct_pass(g, tk);
       if (n >= p.k && n <= p.cap) status = wr.select_candidates(row, n, tk, &kth);
     }
     if (status == 1) {
@@ -770,7 +814,7 @@ __global__ void __launch_bounds__(kWrThreads, 3) topk_warp_rows_kernel(const WrP
       guess = kth > wr_key_floor<ES>() + m ? kth - m : wr_key_floor<ES>();
       have_guess = true;
     } else {
-      wr.exact_row(rowp, row);  // also raises the NaN flag
+      wr.exact_row(g, row);  // also raises the NaN flag
     }
     __syncwarp();
   }

@@ -108,14 +108,20 @@ def test_plan_shapes():
 
 def test_plan_unaligned_rows():
     """Row strides that are not a multiple of 16 bytes put some rows off a
-    16-byte boundary: one CTA per row on the unaligned-rows path, whatever the
-    sizes (a stride of a multiple of 16 bytes keeps the other paths)."""
+    16-byte boundary. Many short rows still take the one-warp-per-row path (it
+    reads the 16-byte blocks overlapping each row); any other such rows take one
+    CTA per row on the unaligned-rows path (a stride of a multiple of 16 bytes
+    keeps the other paths)."""
     for dtype, stride in ((dstk.BF16, 10), (dstk.BF16, 32769), (dstk.FP32, 6), (dstk.FP32, 129281)):
         for batch, k in ((2, 5), (16384, 512), (64, 4)):
             length = stride if stride > 10 else stride - 1
-            rc, p = dstk.ds_topk_plan(dtype, batch, length, stride, min(k, length), 148)
-            assert rc == 0 and p.path == dstk.PATH_UNALIGNED, (dtype, stride, batch)
             kk = min(k, length)
+            rc, p = dstk.ds_topk_plan(dtype, batch, length, stride, kk, 148)
+            warp_rows = length <= 65536 and kk <= 1024 and batch >= min(32, max(4, length // 1024)) * 148
+            if warp_rows:
+                assert rc == 0 and p.path == dstk.PATH_WARP_ROWS, (dtype, stride, batch)
+                continue
+            assert rc == 0 and p.path == dstk.PATH_UNALIGNED, (dtype, stride, batch)
             assert p.cluster_size == 1 and p.grid_ctas == batch
             assert p.granules_per_cta == max(4 * kk + 2048, 8192) and p.smem_bytes == 4 * p.granules_per_cta
             assert p.threads_per_cta == 512 and p.launches == 1
@@ -144,8 +150,9 @@ def test_index_type_checks():
 
 def test_bench_shift_layout_and_plan():
     """bench.py --shift: the copy sits `shift` elements past an aligned start with
-    the same contents, and the plan it reports is the unaligned-rows plan exactly
-    when the shift breaks 16-byte alignment."""
+    the same contents; the decode-shaped batch stays on the one-warp-per-row path
+    at any shift, while the sampler's long rows take the unaligned-rows plan
+    exactly when the shift breaks 16-byte alignment."""
     import torch
 
     import bench
@@ -159,7 +166,7 @@ def test_bench_shift_layout_and_plan():
         else:
             assert y.data_ptr() % 16 == shift * 4 % 16  # the buffer's start is 16-byte aligned
     c4 = workloads.WORKLOADS["c4"]  # bf16 rows of 65536 bytes
-    for shift, path in ((0, dstk.PATH_WARP_ROWS), (1, dstk.PATH_UNALIGNED), (7, dstk.PATH_UNALIGNED),
+    for shift, path in ((0, dstk.PATH_WARP_ROWS), (1, dstk.PATH_WARP_ROWS), (7, dstk.PATH_WARP_ROWS),
                         (8, dstk.PATH_WARP_ROWS)):
         rc, p = bench.plan_for(dstk, c4, 148, shift)
         assert rc == dstk.OK and p.path == path, (shift, p.path)

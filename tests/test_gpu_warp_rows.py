@@ -26,6 +26,11 @@ def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
+def _dstk():
+    import sampler_topk_selection_ds_b300 as dstk
+    return dstk
+
+
 def _wr_batch(length):
     # the path needs min(32, max(4, len / 1024)) rows per SM; +5 leaves a ragged last CTA
     return min(32, max(4, length // 1024)) * _sms() + 5
@@ -144,3 +149,43 @@ def test_warp_rows_candidates_concentrated():
     x[hot, n - 700:] = (x[hot, n - 700:].float() + 8.0).to(torch.bfloat16)
     _assert_path(x, 512)
     assert_parity(x, 512, sorted_index=False, return_value=True)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_warp_rows_rows_off_16_byte_boundaries(dtype):
+    """Many short rows starting at every element offset within a 16-byte block
+    (odd strides, NaN everywhere around the rows, so also inside the first and
+    last blocks the kernel reads): the one-warp-per-row path masks every element
+    outside a row, so clean rows never raise the NaN flag and match the oracle."""
+    from tests.test_gpu_unaligned import place, run_view
+    vec = 16 // (2 if dtype == torch.bfloat16 else 4)
+    for length, k, style in ((1001, 37, "ties"), (4099, 512, "normal"), (30001, 1000, "normal"),
+                             (33, 33, "allequal")):
+        b = _wr_batch(length)
+        x = workloads.random_rows(b, length, dtype, 6100 + length, style=style)
+        for shift, extra in ((1, 1), (vec - 1, 3), (vec // 2, 0)):
+            stride = length + extra
+            dstk = _dstk()
+            dt = dstk.BF16 if dtype == torch.bfloat16 else dstk.FP32
+            rc, plan = dstk.ds_topk_plan(dt, b, length, stride, k, _sms())
+            assert rc == 0 and plan.path == dstk.PATH_WARP_ROWS
+            view = place(x, shift, stride)
+            gv, gi, gf = run_view(view, k, sorted_index=bool(shift % 2), return_value=True)
+            assert gf == 0
+            assert_parity(x, k, bool(shift % 2), True, gpu_out=(gv, gi, gf))
+
+
+def test_warp_rows_off_boundary_nan_and_causal_tail():
+    """Rows off the 16-byte boundary with a -inf tail, and a NaN inside some rows:
+    the flag is raised, the clean rows stay exact."""
+    from tests.test_gpu_unaligned import place, run_view
+    n = 8191
+    b = _wr_batch(n)
+    x = workloads.random_rows(b, n, torch.bfloat16, 6200, style="normal")
+    x[:, 3 * n // 4:] = float("-inf")
+    x[5, 0] = float("nan")
+    x[9, n - 1] = float("nan")
+    view = place(x, 3, n + 1)
+    gv, gi, gf = run_view(view, 512, sorted_index=False, return_value=True)
+    assert gf & 1
+    assert_parity(x, 512, False, True, gpu_out=(gv, gi, gf))
