@@ -59,7 +59,6 @@ _COMMON_SOURCES = [os.path.join(CSRC, "topk_kernel.cuh"), os.path.join(CSRC, "ds
 KERNEL_SOURCES = {
     "topk_rows_kernel": _COMMON_SOURCES,
     "topk_warp_rows_kernel": _COMMON_SOURCES + [os.path.join(CSRC, "warp_rows_kernel.cuh")],
-    "topk_unaligned_kernel": _COMMON_SOURCES + [os.path.join(CSRC, "unaligned_kernel.cuh")],
 }
 
 SAMPLE_TEMPERATURE = 1.0
@@ -68,8 +67,6 @@ SAMPLE_TOP_P = 0.9
 
 def kernel_name(w, plan) -> str:
     es = 2 if w.dtype == torch.bfloat16 else 4
-    if plan.path == 3:
-        return f"topk_unaligned_kernel<{es}>"
     if plan.path == 2:
         return f"topk_warp_rows_kernel<{es}>"
     return f"topk_rows_kernel<{es},{plan.cluster_size}>"
@@ -89,8 +86,9 @@ def shifted(x, shift):
 
 def plan_for(dstk, w, sm_count, shift):
     """The launch plan ds_topk takes for the workload's rows at this shift (the
-    plan call assumes a 16-byte aligned x; a row stride that is not a multiple of
-    16 bytes gives the unaligned-rows plan, which depends on the batch only)."""
+    plan call assumes a 16-byte aligned x, so a shift that breaks 16-byte
+    alignment is stood for by a row stride that is not a multiple of 16 bytes:
+    both put rows off 16-byte boundaries)."""
     stride = w.length
     if (shift * w.elem_size) % 16:
         stride = w.length + 1
@@ -632,7 +630,7 @@ def main(argv=None):
                          "three launches per call)")
     ap.add_argument("--shift", type=int, default=0,
                     help="place the input this many elements past a 16-byte boundary (an odd "
-                         "shift sends every row to the unaligned-rows path)")
+                         "shift puts every row off a 16-byte boundary)")
     ap.add_argument("--case", action="store_true",
                     help="profiling case: run the workload --calls times, untimed (for ncu)")
     ap.add_argument("--rows", type=int, default=0, help="--case: use only the first ROWS rows")

@@ -81,22 +81,24 @@ typedef enum {
  * Arguments (all sizes in ELEMENTS unless stated):
  *   x            device pointer, row-major [batch, row_stride] of `dtype`.
  *                Row b starts at element b*row_stride; elements [0, len) of it
- *                are the row. Only those elements are read (padding
- *                [len, row_stride) is never read nor checked for NaN).
- *                Must be aligned to sizeof(dtype). Rows that start on a
- *                16-byte boundary (x 16-byte aligned and row_stride *
- *                sizeof(dtype) a multiple of 16) take the fast paths; any other
- *                rows take DS_TOPK_PATH_UNALIGNED, which gives the same result
- *                more slowly (one CTA per row; the row is read once to filter
- *                candidates against a guessed threshold, and again from L2 only
- *                when the guess fails or for the ordered output).
+ *                are the row. Only those elements are inspected (padding
+ *                [len, row_stride) is never selected nor checked for NaN).
+ *                Must be aligned to sizeof(dtype); rows need not start on a
+ *                16-byte boundary. Every kernel reads a row as the 16-byte
+ *                aligned blocks that overlap [0, len): the elements of those
+ *                blocks outside the row are masked before any compare (never
+ *                selected nor checked for NaN), and no block without a row
+ *                element is read. Rows off 16-byte boundaries (x not 16-byte
+ *                aligned, or row_stride * sizeof(dtype) not a multiple of 16)
+ *                give the same result; on the one-CTA/cluster-per-row paths
+ *                they forgo the next-row prefetch.
  *   dtype        DS_TOPK_BF16 or DS_TOPK_FP32.
  *   batch        number of rows, >= 0. batch == 0 returns DS_TOPK_OK at once
  *                (pointers may then be NULL).
  *   len          row length, 1 <= len <= INT32_MAX.
- *   row_stride   elements between row starts, >= len. A multiple of 16 bytes
- *                keeps every row on the fast paths (see x); the pages' kernel
- *                requires that alignment and leaves the padding to callers.
+ *   row_stride   elements between row starts, >= len. Any value (see x); the
+ *                pages' kernel requires 16-byte aligned rows and leaves the
+ *                padding to callers, this library does not.
  *   k            1 <= k <= min(len, DS_TOPK_MAX_K).
  *   sorted_index DS_TOPK_SORT_NONE (0), DS_TOPK_SORT_INDEX (1) or
  *                DS_TOPK_SORT_VALUE (2). 1: each output row lists its k indices
@@ -204,13 +206,8 @@ DS_TOPK_API int ds_topk_sample(const void* x, int dtype, int64_t batch, int64_t 
 typedef enum {
   DS_TOPK_PATH_ROW = 0,      /* one CTA per row                                     */
   DS_TOPK_PATH_CLUSTER = 1,  /* one thread-block cluster per row (row split in slices) */
-  DS_TOPK_PATH_WARP_ROWS = 2, /* one warp per row, several rows per CTA: many rows of at
+  DS_TOPK_PATH_WARP_ROWS = 2  /* one warp per row, several rows per CTA: many rows of at
                                  most 65536 elements with k <= 1024                  */
-  DS_TOPK_PATH_UNALIGNED = 3   /* one CTA per row for rows that do not start on a
-                                  16-byte boundary: candidates filtered against a
-                                  guessed threshold into shared memory and radix-
-                                  selected there (exact radix levels over the whole
-                                  row when the guess fails)                        */
 } ds_topk_path;
 
 /* Launch plan of one ds_topk call, as chosen by the host dispatcher. */
@@ -219,17 +216,16 @@ typedef struct {
   int32_t cluster_size;        /* CTAs cooperating on one row (1 for DS_TOPK_PATH_ROW) */
   int32_t threads_per_cta;
   int32_t vectors_per_granule; /* 16-byte vectors summarised by one granule maximum
-                                  (1 on DS_TOPK_PATH_WARP_ROWS and
-                                  DS_TOPK_PATH_UNALIGNED: vectors are tested one by one) */
+                                  (1 on DS_TOPK_PATH_WARP_ROWS: vectors are tested one
+                                  by one)                                              */
   int64_t grid_ctas;           /* CTAs if every row had its own cluster (warp rows: if
                                   every 8 rows had their own CTA), capped at INT32_MAX
-                                  on the warp-rows and unaligned-rows paths; ds_topk
+                                  on the warp-rows path; ds_topk
                                   launches at most as many as can be co-resident, and
                                   each persistent cluster (warp) then walks rows with
                                   a stride                                             */
   int64_t granules_per_cta;    /* size of the per-CTA granule-maximum array; on
-                                  DS_TOPK_PATH_WARP_ROWS the candidate slots per warp,
-                                  on DS_TOPK_PATH_UNALIGNED the candidate slots per CTA */
+                                  DS_TOPK_PATH_WARP_ROWS the candidate slots per warp  */
   int32_t smem_bytes;          /* dynamic shared memory per CTA                        */
   int32_t launches;            /* kernel launches per call with sorted_index 0 or 1
                                   (DS_TOPK_SORT_VALUE adds one)                        */
@@ -239,8 +235,9 @@ typedef struct {
  * ds_topk_plan — fill *plan with the launch plan ds_topk would use for these
  * sizes on a GPU with `sm_count` SMs, without touching the GPU (pure host logic;
  * runs without a device). Same validation as ds_topk for the size arguments
- * (x/output pointers are not involved: x is taken to be 16-byte aligned; an x
- * that is not sends ds_topk to DS_TOPK_PATH_UNALIGNED whatever the plan says).
+ * (x/output pointers are not involved: x is taken to be 16-byte aligned; for an
+ * x that is not, the row/cluster plans may hold one 16-byte block more per row
+ * and no next-row prefetch, the path is the same).
  * Returns DS_TOPK_OK or DS_TOPK_EINVAL; plan must be non-NULL and
  * sm_count >= 1.
  */

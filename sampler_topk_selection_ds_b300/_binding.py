@@ -26,7 +26,6 @@ MAX_K = 4096
 PATH_ROW = 0
 PATH_CLUSTER = 1
 PATH_WARP_ROWS = 2
-PATH_UNALIGNED = 3
 INDEX_INT32 = 0
 INDEX_INT64 = 1
 SORT_NONE = 0   # output order unspecified
@@ -141,10 +140,10 @@ def topk(x: torch.Tensor, k: int, sorted_index=False, return_value: bool = True,
          out: Optional[Tuple[Optional[torch.Tensor], torch.Tensor]] = None,
          stream: Optional[torch.cuda.Stream] = None, index_dtype: torch.dtype = torch.int32):
     """TopK of each row of a CUDA tensor x [batch, row_stride] (row stride may
-    exceed `length`, the number of valid columns; padding is never read). Rows
-    need not start on 16-byte boundaries: such rows (an offset view, or a row
-    stride that is not a multiple of 16 bytes) take the slower unaligned-rows
-    kernel with the same result.
+    exceed `length`, the number of valid columns; padding is never selected nor
+    checked for NaN). Rows need not start on 16-byte boundaries (an offset view,
+    or a row stride that is not a multiple of 16 bytes): every kernel reads a row
+    as the 16-byte blocks that overlap it and masks the elements outside it.
 
     sorted_index: False/True (unspecified / ascending index), or "value"
     (SORT_VALUE: value descending, equal values by ascending index).

@@ -19,7 +19,6 @@
 #include "warp_rows_kernel.cuh"
 #include "value_order_kernel.cuh"
 #include "sampler_kernel.cuh"
-#include "unaligned_kernel.cuh"
 
 namespace {
 
@@ -54,9 +53,7 @@ struct Plan {
   ds_topk_plan_t pub;
   Params prm;
   ds_topk_dev::WrParams wprm;
-  ds_topk_dev::UaParams uprm;
   bool warp_rows;
-  bool unaligned;
   int es;
 };
 
@@ -85,7 +82,6 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
   const int64_t nvec = ceil_div(len, vec);
   const int64_t row_bytes = len * es;
   out->warp_rows = false;
-  out->unaligned = false;
 
   // Many short rows: one warp per row (candidate indices fit 16 bits, and a
   // warp's candidate buffer of about 2k entries leaves room for 2+ CTAs per SM).
@@ -144,40 +140,12 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
     }
   }
 
-  // Rows that do not all start on a 16-byte boundary: one CTA per row, radix
-  // selection over the aligned vectors that overlap the row.
-  if (!x_aligned || (row_stride * es) % 16 != 0) {
-    out->es = es;
-    out->unaligned = true;
-    ds_topk_plan_t& pl = out->pub;
-    pl.path = DS_TOPK_PATH_UNALIGNED;
-    pl.cluster_size = 1;
-    pl.threads_per_cta = ds_topk_dev::kUaThreads;
-    pl.vectors_per_granule = 1;
-    // candidate keys of a guessed threshold (about 1.5 k expected; also holds
-    // the first-row sample)
-    int64_t cap = 4 * static_cast<int64_t>(k) + 2048;
-    if (cap < ds_topk_dev::kUaSampleKeys) cap = ds_topk_dev::kUaSampleKeys;
-    // persistent: each CTA walks rows with a stride of the grid, so the grid may
-    // be capped at the largest launchable size
-    pl.grid_ctas = batch < INT32_MAX ? batch : INT32_MAX;
-    pl.granules_per_cta = cap;
-    pl.smem_bytes = static_cast<int32_t>(cap * 4);
-    pl.launches = batch > 0 ? 1 : 0;
-    ds_topk_dev::UaParams& u = out->uprm;
-    u.x = nullptr;
-    u.batch = batch;
-    u.row_stride_bytes = row_stride * es;
-    u.len = len;
-    u.k = k;
-    u.cap = static_cast<int32_t>(cap);
-    u.return_value = 0;
-    u.out_values = nullptr;
-    u.out_indices = nullptr;
-    u.idx64 = 0;
-    u.flag = nullptr;
-    return DS_TOPK_OK;
-  }
+  // Rows that do not all start on a 16-byte boundary are read as the 16-byte
+  // blocks that overlap them: up to one block more than an aligned row, and no
+  // next-row prefetch (its copies need aligned rows).
+  const bool rows_aligned = x_aligned && (row_stride * es) % 16 == 0;
+  const int64_t nvec_cov = rows_aligned ? nvec : ceil_div(len + vec - 1, vec);
+  if (!rows_aligned) stage = false;
 
   int S = 1;
   if (row_bytes > kSplitMinRowBytes && batch < 2 * static_cast<int64_t>(sm_count)) {
@@ -187,13 +155,13 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
     if (S < 2 && by_size >= 2 && want >= 2) S = 2;
     if (S > max_cluster) S = max_cluster;
   }
-  const int64_t vec_per_cta = ceil_div(nvec, S);
+  const int64_t vec_per_cta = ceil_div(nvec_cov, S);
   const int64_t gv = ceil_div(vec_per_cta, kGranuleCap);
   const int64_t g_cap = ceil_div(vec_per_cta, gv);
   const int64_t g_cap_pad = (g_cap + 7) & ~int64_t(7);
   int64_t g_total = 0;
   for (int r = 0; r < S; ++r) {
-    int64_t n = nvec - r * vec_per_cta;
+    int64_t n = nvec_cov - r * vec_per_cta;
     if (n > vec_per_cta) n = vec_per_cta;
     if (n > 0) g_total += ceil_div(n, gv);
   }
@@ -254,7 +222,7 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
   p.batch = batch;
   p.row_stride_bytes = row_stride * es;
   p.len = len;
-  p.nvec = nvec;
+  p.nvec = nvec_cov;
   p.vec_per_cta = vec_per_cta;
   p.g_total = g_total;
   p.gv = static_cast<int32_t>(gv);
@@ -310,11 +278,6 @@ cudaError_t prepare_dtype() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(ds_topk_dev::topk_warp_rows_kernel<ES>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
-  // the unaligned-rows kernel's largest candidate buffer (k = DS_TOPK_MAX_K); it
-  // also has static shared memory, so the full per-CTA limit would be refused
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(ds_topk_dev::topk_unaligned_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (4 * DS_TOPK_MAX_K + 2048) * 4);
   return e;
 }
 
@@ -420,30 +383,18 @@ int resident_warp_rows(int smem, int sm_count) {
   return n * sm_count;
 }
 
-template <int ES>
-int resident_unaligned(int smem, int sm_count) {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ds_topk_dev::topk_unaligned_kernel<ES>,
-                                                    ds_topk_dev::kUaThreads, smem) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n * sm_count;
-}
-
 // Cached resident_clusters() per (device, dtype, cluster size, variant, shared memory);
-// the warp-rows kernel is cached as variant 2, the unaligned-rows kernel as 3.
+// the warp-rows kernel is cached as variant 2.
 int resident_cached(int dev, const Plan& pl, int sm_count) {
   const int es = pl.es, S = pl.pub.cluster_size, smem = pl.pub.smem_bytes;
-  const int gv1 = pl.unaligned ? 3 : pl.warp_rows ? 2 : (pl.prm.gv == 1 ? 1 : 0);
+  const int gv1 = pl.warp_rows ? 2 : (pl.prm.gv == 1 ? 1 : 0);
   std::lock_guard<std::mutex> lock(g_mu);
   for (int i = 0; i < g_residency_used; ++i) {
     const ResidencyEntry& e = g_residency[i];
     if (e.dev == dev && e.es == es && e.S == S && e.gv1 == gv1 && e.smem == smem) return e.clusters;
   }
   int n;
-  if (gv1 == 3) n = es == 2 ? resident_unaligned<2>(smem, sm_count) : resident_unaligned<4>(smem, sm_count);
-  else if (gv1 == 2) n = es == 2 ? resident_warp_rows<2>(smem, sm_count) : resident_warp_rows<4>(smem, sm_count);
+  if (gv1 == 2) n = es == 2 ? resident_warp_rows<2>(smem, sm_count) : resident_warp_rows<4>(smem, sm_count);
   else if (es == 2) n = gv1 ? resident_variant<2, true>(S, smem, sm_count) : resident_variant<2, false>(S, smem, sm_count);
   else n = gv1 ? resident_variant<4, true>(S, smem, sm_count) : resident_variant<4, false>(S, smem, sm_count);
   if (g_residency_used < kResidencySlots) g_residency[g_residency_used++] = {dev, es, S, gv1, smem, n};
@@ -504,19 +455,7 @@ cudaError_t launch_warp_rows(const Plan& pl, cudaStream_t stream) {
 }
 
 template <int ES>
-cudaError_t launch_unaligned(const Plan& pl, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(pl.pub.grid_ctas), 1, 1);
-  cfg.blockDim = dim3(ds_topk_dev::kUaThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(pl.pub.smem_bytes);
-  cfg.stream = stream;
-  cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, ds_topk_dev::topk_unaligned_kernel<ES>, pl.uprm);
-}
-
-template <int ES>
 cudaError_t launch_dtype(const Plan& pl, cudaStream_t stream) {
-  if (pl.unaligned) return launch_unaligned<ES>(pl, stream);
   if (pl.warp_rows) return launch_warp_rows<ES>(pl, stream);
   return pl.prm.gv == 1 ? launch_variant<ES, true>(pl, stream) : launch_variant<ES, false>(pl, stream);
 }
@@ -607,24 +546,6 @@ extern "C" int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, 
   // persistent cluster walks several rows); otherwise without it.
   rc = make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, false, x_aligned, &pl);
   if (rc != DS_TOPK_OK) return rc;
-  if (pl.unaligned) {
-    pl.uprm.x = static_cast<const char*>(x);
-    pl.uprm.return_value = return_value;
-    pl.uprm.out_values = return_value ? out_values : nullptr;
-    pl.uprm.out_indices = out_indices;
-    pl.uprm.idx64 = idx64;
-    pl.uprm.flag = nan_flag;
-    // every resident CTA walks rows with a stride of the grid
-    const int resident_ctas = resident_cached(dev_id, pl, dev.sm_count);
-    if (resident_ctas > 0 && pl.pub.grid_ctas > resident_ctas) pl.pub.grid_ctas = resident_ctas;
-    const cudaError_t e = es == 2 ? launch_dtype<2>(pl, stream) : launch_dtype<4>(pl, stream);
-    if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) {
-      cudaGetLastError();
-      return DS_TOPK_ECUDA;
-    }
-    return finish_order(es, sorted_index, x, batch, len, row_stride, k, return_value, out_values, out_indices,
-                        idx64, dev.sm_count, stream);
-  }
   if (pl.warp_rows) {
     pl.wprm.x = static_cast<const char*>(x);
     pl.wprm.return_value = return_value;
@@ -645,7 +566,7 @@ extern "C" int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, 
   int resident = resident_cached(dev_id, pl, dev.sm_count);
   if (resident > 0 && batch > resident) {
     Plan ps;
-    if (make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, true, true, &ps) ==
+    if (make_plan(dtype, batch, len, row_stride, k, dev.sm_count, dev.max_cluster, true, x_aligned, &ps) ==
             DS_TOPK_OK &&
         ps.prm.stage_vecs > 0) {
       const int rs = resident_cached(dev_id, ps, dev.sm_count);

@@ -99,29 +99,32 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return r;
 }
 
-// Vector v of a row (elements [v*VEC, v*VEC+VEC)). Elements at or beyond len are
-// not read; their lanes hold -inf (only maxima see them; every element pass
-// also tests the index against len).
+// Block v of a row read as 16-byte aligned blocks (rowp: the row's first block;
+// the row's element i is element i + lead of that sequence; nvr blocks overlap
+// the row): elements outside the row read as -inf, and a block past the row is
+// not read at all. A block holding any row element is read whole (an aligned
+// 16-byte block never crosses a page).
 template <int ES>
-__device__ __forceinline__ uint4 load_vec(const char* rowp, int64_t v, int64_t len) {
+__device__ __forceinline__ uint4 load_blk(const char* rowp, int64_t v, int lead, int64_t len, int64_t nvr) {
   constexpr int VEC = Traits<ES>::kVec;
-  const int64_t e0 = v * VEC;
-  if (e0 + VEC <= len) return ld_nc_v4(rowp + v * 16);
-  uint32_t w[4] = {Traits<ES>::kNegInfWord, Traits<ES>::kNegInfWord, Traits<ES>::kNegInfWord,
-                   Traits<ES>::kNegInfWord};
+  constexpr uint32_t NI = Traits<ES>::kNegInfWord;
+  if (v >= nvr) return make_uint4(NI, NI, NI, NI);
+  uint4 w = ld_nc_v4(rowp + v * 16);
+  const int64_t e0 = v * VEC - lead;  // row index of the block's element 0
+  if (e0 >= 0 && e0 + VEC <= len) return w;
+  uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
   for (int e = 0; e < VEC; ++e) {
-    if (e0 + e < len) {
+    if (e0 + e < 0 || e0 + e >= len) {
       if constexpr (ES == 2) {
-        const uint32_t h = *reinterpret_cast<const uint16_t*>(rowp + (e0 + e) * 2);
         const int sh = (e & 1) * 16;
-        w[e >> 1] = (w[e >> 1] & ~(0xFFFFu << sh)) | (h << sh);
+        ws[e >> 1] = (ws[e >> 1] & ~(0xFFFFu << sh)) | ((NI & 0xFFFFu) << sh);
       } else {
-        w[e] = *reinterpret_cast<const uint32_t*>(rowp + (e0 + e) * 4);
+        ws[e] = NI;
       }
     }
   }
-  return make_uint4(w[0], w[1], w[2], w[3]);
+  return make_uint4(ws[0], ws[1], ws[2], ws[3]);
 }
 
 template <int ES>
@@ -598,7 +601,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
   // cp.async while the previous row is being selected (each thread copies and
   // later reads only its own slots, so no barrier is needed around them).
   const int nsteps = (se - sb + 31) / 32;
-  const int nstage = gv == 1 ? min(p.stage_vecs, nsteps) : 0;
+  // (only rows on 16-byte boundaries: the copies are 16-byte cp.async)
+  const bool rows_aligned = (reinterpret_cast<uintptr_t>(p.x) % 16 == 0) && (p.row_stride_bytes % 16 == 0);
+  const int nstage = (gv == 1 && rows_aligned) ? min(p.stage_vecs, nsteps) : 0;
   auto prefetch = [&](int64_t r) {
     const uint4* src = reinterpret_cast<const uint4*>(p.x + r * p.row_stride_bytes) + v0;
     for (int i = 0; i < nstage; ++i) {
@@ -622,8 +627,17 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
 
 #pragma unroll 1
   for (int64_t row = blockIdx.x / S; row < p.batch; row += row_step) {
-    const char* rowp = p.x + row * p.row_stride_bytes;
+    // the row as 16-byte aligned blocks: its element i is element i + lead of
+    // block 0; blocks [vf0, vf1) lie wholly inside it, nvr blocks overlap it
+    // (a row that starts on a 16-byte boundary has lead 0)
+    const uintptr_t raddr = reinterpret_cast<uintptr_t>(p.x + row * p.row_stride_bytes);
+    const char* rowp = reinterpret_cast<const char*>(raddr & ~static_cast<uintptr_t>(15));
     const uint4* rowv = reinterpret_cast<const uint4*>(rowp);
+    const int lead = static_cast<int>((raddr & 15u) / ES);
+    const int64_t nvr = (lead + p.len + VEC - 1) / VEC;
+    const int gf0 = (lead != 0 && v0 == 0) ? 1 : 0;  // slice blocks [gf0, Gfr) are whole
+    const int Gfr = gv == 1 ? static_cast<int>(max(int64_t(0), min(nv, (lead + p.len) / VEC - v0))) : G;
+    auto blk = [&](int64_t v) -> uint4 { return load_blk<ES>(rowp, v, lead, p.len, nvr); };
     if (tid == 0) {  // level results start defined even if a NaN row breaks the counts
       bc[0] = 0;
       bc[1] = 0;
@@ -658,14 +672,14 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           for (int u = 0; u < U; ++u) {
             const int i = i0 + u;
             const int g = sb + 32 * i + lane;
-            if (g < min(se, Gf)) {
+            if (g >= gf0 && g < min(se, Gfr)) {
               if (staged && i < nstage) {
                 w[u] = stage[i * kThreads + tid];
               } else {
                 w[u] = ld_nc_v4(rowv + (v0 + g));
               }
             } else if (g < se) {
-              w[u] = load_vec<ES>(rowp, v0 + g, p.len);  // ragged last vector
+              w[u] = blk(v0 + g);  // a block the row only partly covers
             }
           }
 #pragma unroll
@@ -703,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           if (ok) {
             const int64_t vb = v0 + static_cast<int64_t>(g) * gv;
             const int64_t ve = min(vb + gv, v1);
-            for (int64_t v = vb; v < ve; ++v) acc = max_acc<ES>(acc, load_vec<ES>(rowp, v, p.len));
+            for (int64_t v = vb; v < ve; ++v) acc = max_acc<ES>(acc, blk(v));
           }
           nan_acc = max_packed<ES>(nan_acc, acc);
           const uint32_t raw = finish_max<ES>(acc);
@@ -847,18 +861,20 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     const uint32_t tv2 = (__float_as_uint(tval) >> 16) * 0x00010001u;  // bf16 bits, both halves
     const uint4* slice = rowv + v0;
     const int nvs = static_cast<int>(nv);  // vectors in this slice
-    const int nfull = gv == 1 ? Gf : static_cast<int>(max(int64_t(0), min(nv, p.len / VEC - v0)));
+    const int nfull = gv == 1 ? Gfr : static_cast<int>(max(int64_t(0), min(nv, (lead + p.len) / VEC - v0)));
     // candidate mask of slice vector v (ragged last vector: lanes past len cleared)
     auto vmask_of = [&](int v, const uint4& w) -> uint32_t {
       uint32_t m = cand_mask<ES>(w, tval, tv2);
-      if (v >= nfull) {
-        const int64_t valid = p.len - (v0 + v) * VEC;
-        m &= valid <= 0 ? 0u : (valid >= VEC ? 0xFFu : ((1u << valid) - 1u));
+      if (v < gf0 || v >= nfull) {  // only the row's elements of a partly covered block
+        const int64_t e0 = (v0 + v) * VEC - lead;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+          if (e0 + e < 0 || e0 + e >= p.len) m &= ~(1u << e);
       }
       return m;
     };
     auto load_slice = [&](int v) -> uint4 {
-      return v < nfull ? ld_nc_v4(slice + v) : load_vec<ES>(rowp, v0 + v, p.len);
+      return (v >= gf0 && v < nfull) ? ld_nc_v4(slice + v) : blk(v0 + v);
     };
     const int ncache = gv == 1 ? min(lc, p.lvec_cap) : 0;  // list entries held in wvec
     // Every listed granule holds at least one candidate, so a CTA whose listed
@@ -945,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
             w = load_slice(v);
             m = vmask_of(v, w);
           }
-          const uint32_t ibase = static_cast<uint32_t>((v0 + v) * VEC);
+          const uint32_t ibase = static_cast<uint32_t>((v0 + v) * VEC - lead);
           while (m) {
             const int e = __ffs(m) - 1;
             m &= m - 1;
@@ -1226,6 +1242,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         if (gv == 1) {  // 4 listed vectors in flight per lane (row vector indices fit 32 bits)
           constexpr int UV = 4;
           const int ilen = static_cast<int>(p.len);
+          const int ilead = lead;
           for (int jb = 0; jb < lcnt; jb += 32 * UV) {
             uint4 w[UV];
             int v[UV];
@@ -1234,7 +1251,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
               const int j = jb + 32 * u + lane;
               v[u] = j < lcnt ? vec_at(j) : -1;
               w[u] = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
-              if (v[u] >= 0) w[u] = load_vec<ES>(rowp, v[u], p.len);
+              if (v[u] >= 0) w[u] = blk(v[u]);
             }
 #pragma unroll
             for (int u = 0; u < UV; ++u) {
@@ -1243,7 +1260,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
               for (int e = 0; e < VEC; ++e) {
                 const uint32_t eb = elem_bits<ES>(w[u], e);
                 const uint32_t key = key_of<ES>(eb);
-                f(key, vok && (v[u] * VEC + e < ilen) && (key >= T_full || is_nan_bits<ES>(eb)));
+                const int idx = v[u] * VEC + e - ilead;
+                f(key, vok && idx >= 0 && idx < ilen && (key >= T_full || is_nan_bits<ES>(eb)));
               }
             }
           }
@@ -1255,12 +1273,13 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
             const int64_t v = gok ? v0 + static_cast<int64_t>(wlist[j]) * gv + q : v1;
             const bool vok = v < v1;
             uint4 w = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
-            if (vok) w = load_vec<ES>(rowp, v, p.len);
+            if (vok) w = blk(v);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
               const uint32_t eb = elem_bits<ES>(w, e);
               const uint32_t key = key_of<ES>(eb);
-              f(key, vok && (v * VEC + e < p.len) && (key >= T_full || is_nan_bits<ES>(eb)));
+              const int64_t idx = v * VEC + e - lead;
+              f(key, vok && idx >= 0 && idx < p.len && (key >= T_full || is_nan_bits<ES>(eb)));
             }
           }
         }
@@ -1372,7 +1391,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         for (int e = 0; e < VEC; ++e) {
           const uint32_t eb = elem_bits<ES>(w, e);
           const uint32_t key = key_of<ES>(eb);
-          if (vok && v * VEC + e < p.len && (key >= T_full || is_nan_bits<ES>(eb))) {
+          const int64_t ix = v * VEC + e - lead;
+          if (vok && ix >= 0 && ix < p.len && (key >= T_full || is_nan_bits<ES>(eb))) {
             lg += key > kstar;
             lq += key == kstar;
           }
@@ -1384,10 +1404,10 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         if (lg + lq == 0) return;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-          const int64_t idx = v * VEC + e;
+          const int64_t idx = v * VEC + e - lead;
           const uint32_t bits = elem_bits<ES>(w, e);
           const uint32_t key = key_of<ES>(bits);
-          if (vok && idx < p.len && (key >= T_full || is_nan_bits<ES>(bits))) {
+          if (vok && idx >= 0 && idx < p.len && (key >= T_full || is_nan_bits<ES>(bits))) {
             uint32_t pos = 0xFFFFFFFFu;
             if (key > kstar) {
               pos = bg + min(bq, r_ties);
@@ -1415,7 +1435,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
             const int j = jb + 32 * u + lane;
             v[u] = j < lcnt ? static_cast<int64_t>(vec_at(j)) : -1;
             w[u] = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
-            if (v[u] >= 0) w[u] = load_vec<ES>(rowp, v[u], p.len);
+            if (v[u] >= 0) w[u] = blk(v[u]);
           }
 #pragma unroll
           for (int u = 0; u < UV; ++u) write_vec(w[u], v[u], v[u] >= 0);
@@ -1428,7 +1448,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           for (int q = 0; q < gv; ++q) {
             const int64_t v = gok ? v0 + static_cast<int64_t>(wlist[j]) * gv + q : v1;
             uint4 w = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
-            if (v < v1) w = load_vec<ES>(rowp, v, p.len);
+            if (v < v1) w = blk(v);
             write_vec(w, v, v < v1);
           }
         }

@@ -107,28 +107,31 @@ def test_plan_shapes():
     assert dstk.ds_topk_plan(dstk.FP32, 1, 10, 12, 5, 0)[0] == dstk.EINVAL
 
 def test_plan_unaligned_rows():
-    """Row strides that are not a multiple of 16 bytes put some rows off a
-    16-byte boundary. Many short rows still take the one-warp-per-row path (it
-    reads the 16-byte blocks overlapping each row); any other such rows take one
-    CTA per row on the unaligned-rows path (a stride of a multiple of 16 bytes
-    keeps the other paths)."""
+    """Row strides that are not a multiple of 16 bytes put rows off 16-byte
+    boundaries. Every path reads such rows as the 16-byte blocks that overlap
+    them, so the path is chosen from the sizes alone, as for aligned rows: many
+    short rows take one warp per row, others one CTA or cluster per row, with
+    up to one block more per row and no next-row prefetch."""
     for dtype, stride in ((dstk.BF16, 10), (dstk.BF16, 32769), (dstk.FP32, 6), (dstk.FP32, 129281)):
+        es = 2 if dtype == dstk.BF16 else 4
         for batch, k in ((2, 5), (16384, 512), (64, 4)):
             length = stride if stride > 10 else stride - 1
             kk = min(k, length)
             rc, p = dstk.ds_topk_plan(dtype, batch, length, stride, kk, 148)
+            assert rc == 0
             warp_rows = length <= 65536 and kk <= 1024 and batch >= min(32, max(4, length // 1024)) * 148
             if warp_rows:
-                assert rc == 0 and p.path == dstk.PATH_WARP_ROWS, (dtype, stride, batch)
+                assert p.path == dstk.PATH_WARP_ROWS, (dtype, stride, batch)
                 continue
-            assert rc == 0 and p.path == dstk.PATH_UNALIGNED, (dtype, stride, batch)
-            assert p.cluster_size == 1 and p.grid_ctas == batch
-            assert p.granules_per_cta == max(4 * kk + 2048, 8192) and p.smem_bytes == 4 * p.granules_per_cta
-            assert p.threads_per_cta == 512 and p.launches == 1
-    rc, p = dstk.ds_topk_plan(dstk.BF16, 2, 10, 16, 5, 148)  # 32-byte stride: fast path
+            assert p.path in (dstk.PATH_ROW, dstk.PATH_CLUSTER), (dtype, stride, batch)
+            # the CTAs' slices cover every 16-byte block a row off the boundary can overlap
+            vec = 16 // es
+            blocks = -(-(length + vec - 1) // vec)
+            assert p.cluster_size * p.granules_per_cta * p.vectors_per_granule >= blocks
+    rc, p = dstk.ds_topk_plan(dstk.BF16, 2, 10, 16, 5, 148)  # 32-byte stride
     assert rc == 0 and p.path == dstk.PATH_ROW
     rc, p = dstk.ds_topk_plan(dstk.FP32, 0, 10, 10, 5, 148)
-    assert rc == 0 and p.path == dstk.PATH_UNALIGNED and p.launches == 0
+    assert rc == 0 and p.launches == 0
 
 
 def test_binding_has_no_cpu_fallback():
@@ -150,9 +153,8 @@ def test_index_type_checks():
 
 def test_bench_shift_layout_and_plan():
     """bench.py --shift: the copy sits `shift` elements past an aligned start with
-    the same contents; the decode-shaped batch stays on the one-warp-per-row path
-    at any shift, while the sampler's long rows take the unaligned-rows plan
-    exactly when the shift breaks 16-byte alignment."""
+    the same contents; each workload keeps its path at any shift (the decode-
+    shaped batch one warp per row, the sampler's long rows a cluster per row)."""
     import torch
 
     import bench
@@ -170,11 +172,10 @@ def test_bench_shift_layout_and_plan():
                         (8, dstk.PATH_WARP_ROWS)):
         rc, p = bench.plan_for(dstk, c4, 148, shift)
         assert rc == dstk.OK and p.path == path, (shift, p.path)
-        assert bench.kernel_name(c4, p).startswith("topk_unaligned" if path == dstk.PATH_UNALIGNED
-                                                   else "topk_warp_rows")
+        assert bench.kernel_name(c4, p).startswith("topk_warp_rows")
     c2 = workloads.WORKLOADS["c2"]  # fp32: a 4-element shift keeps 16-byte alignment
     assert bench.plan_for(dstk, c2, 148, 4)[1].path == dstk.PATH_CLUSTER
-    assert bench.plan_for(dstk, c2, 148, 2)[1].path == dstk.PATH_UNALIGNED
+    assert bench.plan_for(dstk, c2, 148, 2)[1].path == dstk.PATH_CLUSTER
 
 
 def test_bench_kernel_hash_ignores_comments_only():
@@ -186,9 +187,8 @@ def test_bench_kernel_hash_ignores_comments_only():
         '/* a note */ int f(int a)  {\n  return a + 1;  // two\n}\nconst char* s = "a // b";')
     assert bench.code_only(base) != bench.code_only(base.replace("a + 1", "a + 2"))
     assert bench.code_only(base) != bench.code_only(base.replace('"a // b"', '"a // c"'))
-    hashes = {bench.kernel_hash(k) for k in ("topk_rows_kernel<4,4>", "topk_warp_rows_kernel<2>",
-                                             "topk_unaligned_kernel<2>")}
-    assert len(hashes) == 3
+    hashes = {bench.kernel_hash(k) for k in ("topk_rows_kernel<4,4>", "topk_warp_rows_kernel<2>")}
+    assert len(hashes) == 2
 
 
 def test_bench_traffic_table():
@@ -208,7 +208,7 @@ def test_bench_traffic_table():
             assert t == e["dram_bytes_per_launch"]
         else:
             assert t is None and note.startswith("stale")
-        other = "topk_unaligned_kernel<2>" if not e["kernel"].startswith("topk_unaligned") else "topk_rows_kernel<4,4>"
+        other = "topk_warp_rows_kernel<4>" if not e["kernel"].startswith("topk_warp_rows") else "topk_rows_kernel<4,4>"
         assert bench.profiled_traffic(wl, other)[0] is None
     assert bench.profiled_traffic("no-such-workload", "topk_rows_kernel<4,4>")[0] is None
 

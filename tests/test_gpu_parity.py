@@ -34,7 +34,7 @@ def _aligned(x, length):
     """Rows whose byte length is not a multiple of 16 are copied into a padded
     buffer (NaN padding, which must never be read), so that these tests run the
     paths for rows on 16-byte boundaries; rows off those boundaries are covered
-    by test_gpu_unaligned.py."""
+    by test_gpu_unaligned.py and test_gpu_warp_rows.py."""
     es = x.element_size()
     if x.stride(0) * es % 16 == 0 or x.shape[0] == 1:
         return x, length

@@ -1,5 +1,6 @@
-"""GPU parity of rows that do not start on a 16-byte boundary (the unaligned-rows
-path) against the CPU oracle, bit-exact.
+"""GPU parity of rows that do not start on a 16-byte boundary against the CPU
+oracle, bit-exact (every path reads such rows as the 16-byte blocks that
+overlap them and masks the elements outside the row).
 
 Rows are placed in a NaN-filled device buffer at an element offset (`shift`)
 and with a row stride that need not be a multiple of 16 bytes, so row starts
@@ -64,7 +65,9 @@ def check(x_cpu, k, shift, stride, sorted_index=False, return_value=True):
 def test_plan_reports_the_path():
     dstk = _dstk()
     rc, p = dstk.ds_topk_plan(dstk.BF16, 64, 1001, 1001, 64, 148)
-    assert rc == 0 and p.path == dstk.PATH_UNALIGNED
+    assert rc == 0 and p.path == dstk.PATH_ROW
+    rc, p = dstk.ds_topk_plan(dstk.FP32, 64, 129281, 129281, 512, 148)
+    assert rc == 0 and p.path == dstk.PATH_CLUSTER
 
 
 UA_SWEEP = [
