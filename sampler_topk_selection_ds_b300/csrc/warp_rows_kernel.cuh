@@ -541,6 +541,50 @@ struct WarpRow {
     }
   }
 
+  // ---- C: the ordered output pass --------------------------------------------------
+  // Every candidate with key > kth, and the first `need` with key == kth in index
+  // order, written at consecutive positions of the row's output (ascending index).
+  template <bool IDX64, bool RETV>
+  __device__ __forceinline__ void write_out(int64_t row, int n, uint32_t kth, uint32_t need) const {
+    using VT = typename std::conditional<ES == 2, uint16_t, uint32_t>::type;
+    const int64_t obase = row * p.k;
+    int32_t* oi32 = static_cast<int32_t*>(p.out_indices) + obase;
+    int64_t* oi64 = static_cast<int64_t*>(p.out_indices) + obase;
+    VT* ov = RETV ? static_cast<VT*>(p.out_values) + obase : nullptr;
+    int taken_eq = 0, out = 0;
+    for (int j0 = 0; j0 < n && out < p.k; j0 += 32 * kSelU) {
+      uint32_t wv[kSelU], gtb[kSelU], eqb[kSelU];
+#pragma unroll
+      for (int u = 0; u < kSelU; ++u) {
+        const int j = j0 + 32 * u + lane;
+        wv[u] = j < n ? cw[j] : 0u;  // bf16: bits | index << 16; fp32: bits
+      }
+#pragma unroll
+      for (int u = 0; u < kSelU; ++u) {
+        const bool in = j0 + 32 * u + lane < n;
+        const uint32_t key = key_of<ES>(ES == 2 ? (wv[u] & 0xFFFFu) : wv[u]);
+        gtb[u] = __ballot_sync(kFull, in && key > kth);
+        eqb[u] = __ballot_sync(kFull, in && key == kth);
+      }
+#pragma unroll
+      for (int u = 0; u < kSelU; ++u) {
+        const bool eq = (eqb[u] >> lane) & 1u;
+        const bool sel = ((gtb[u] >> lane) & 1u) ||
+                         (eq && static_cast<uint32_t>(taken_eq + __popc(eqb[u] & lt)) < need);
+        taken_eq += __popc(eqb[u]);
+        const uint32_t sb = __ballot_sync(kFull, sel);
+        const int o = out + __popc(sb & lt);
+        if (sel && o < p.k) {
+          const int idx = ES == 2 ? static_cast<int>(wv[u] >> 16) : static_cast<int>(ci[j0 + 32 * u + lane]);
+          if (IDX64) oi64[o] = idx;
+          else oi32[o] = idx;
+          if (RETV) ov[o] = static_cast<VT>(ES == 2 ? (wv[u] & 0xFFFFu) : wv[u]);
+        }
+        out += __popc(sb);
+      }
+    }
+  }
+
   // ---- R + C on the candidates ---------------------------------------------------
   // n candidates (k <= n <= cap), every non-NaN one with key >= tk, in index
   // order. Writes the row's top k and returns 1 with the k-th key in *kth, or
@@ -604,40 +648,12 @@ struct WarpRow {
     }
     const uint32_t kth = lo;
     // ordered output: ties (key == kth) are taken in index order, `need` of them
-    int taken_eq = 0, out = 0;
-    const int64_t obase = row * p.k;
-    for (int j0 = 0; j0 < n && out < p.k; j0 += 32 * kSelU) {
-      uint32_t bits[kSelU], gtb[kSelU], eqb[kSelU];
-#pragma unroll
-      for (int u = 0; u < kSelU; ++u) {
-        const int j = j0 + 32 * u + lane;
-        bits[u] = j < n ? bits_at(j) : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < kSelU; ++u) {
-        const bool in = j0 + 32 * u + lane < n;
-        const uint32_t key = key_of<ES>(bits[u]);
-        gtb[u] = __ballot_sync(kFull, in && key > kth);
-        eqb[u] = __ballot_sync(kFull, in && key == kth);
-      }
-#pragma unroll
-      for (int u = 0; u < kSelU; ++u) {
-        // ties are taken in index order while fewer than `need` are taken
-        const bool eq = (eqb[u] >> lane) & 1u;
-        const bool sel = ((gtb[u] >> lane) & 1u) ||
-                         (eq && static_cast<uint32_t>(taken_eq + __popc(eqb[u] & lt)) < need);
-        taken_eq += __popc(eqb[u]);
-        const uint32_t sb = __ballot_sync(kFull, sel);
-        if (sel && out + __popc(sb & lt) < p.k) {
-          const int64_t o = obase + out + __popc(sb & lt);
-          put_index(p.out_indices, o, idx_at(j0 + 32 * u + lane), p.idx64);
-          if (p.return_value) {
-            if constexpr (ES == 2) static_cast<uint16_t*>(p.out_values)[o] = static_cast<uint16_t>(bits[u]);
-            else static_cast<uint32_t*>(p.out_values)[o] = bits[u];
-          }
-        }
-        out += __popc(sb);
-      }
+    if (p.idx64) {
+      if (p.return_value) write_out<true, true>(row, n, kth, need);
+      else write_out<true, false>(row, n, kth, need);
+    } else {
+      if (p.return_value) write_out<false, true>(row, n, kth, need);
+      else write_out<false, false>(row, n, kth, need);
     }
     *kth_out = kth;
     return 1;
