@@ -22,6 +22,17 @@
 //      elements with key == K* until k are taken, written in ascending index
 //      order (so sorted_index costs nothing).
 //
+// When some CTA's candidates overflow its buffer (heavy ties, sorted, ramp or
+// few-level rows), B and C run over the listed granules instead, re-read from
+// L2, after the listed granules are spread evenly over every warp of the
+// cluster (a sorted row lists only its top, which one CTA holds).
+//
+// A row may start at any element offset: it is read as the 16-byte aligned
+// blocks that overlap it (its element i is element i + lead of the first
+// block). Blocks wholly inside the row take the fast 16-byte path; the elements
+// of the two partial blocks that lie outside the row read as -inf, and a block
+// past the row is never read.
+//
 // Sources: deepseek.csdn.net, "DeepSeek 一次开源三个仓库", section 三 (算子层): the
 // selection of each row's top K and its threshold/candidate scheme;
 // deepseek-v4-pro.uk (zh-tw), "深入 DeepSeek V4.1 全新開放推論工具包", section
@@ -862,7 +873,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
     const uint4* slice = rowv + v0;
     const int nvs = static_cast<int>(nv);  // vectors in this slice
     const int nfull = gv == 1 ? Gfr : static_cast<int>(max(int64_t(0), min(nv, (lead + p.len) / VEC - v0)));
-    // candidate mask of slice vector v (ragged last vector: lanes past len cleared)
+    // candidate mask of slice vector v (in a block the row only partly covers,
+    // the elements outside the row are cleared)
     auto vmask_of = [&](int v, const uint4& w) -> uint32_t {
       uint32_t m = cand_mask<ES>(w, tval, tv2);
       if (v < gf0 || v >= nfull) {  // only the row's elements of a partly covered block
