@@ -103,8 +103,9 @@ typedef enum {
  *   sorted_index DS_TOPK_SORT_NONE (0), DS_TOPK_SORT_INDEX (1) or
  *                DS_TOPK_SORT_VALUE (2). 1: each output row lists its k indices
  *                in ascending index order. 0: the order within a row is
- *                unspecified (this implementation emits ascending index order,
- *                because its ordered compaction produces it at no extra cost).
+ *                unspecified (the one-CTA/cluster paths emit ascending index
+ *                order anyway; the one-warp-per-row path writes the elements
+ *                above the k-th value first and the ties at it last).
  *                2: value descending, equal values by ascending index (the
  *                selection's total order); this costs one more kernel launch on
  *                the same stream, a per-row sort of the k outputs

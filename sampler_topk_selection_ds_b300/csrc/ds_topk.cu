@@ -132,6 +132,7 @@ int make_plan(int dtype, int64_t batch, int64_t len, int64_t row_stride, int k, 
       w.depth = depth;
       w.k = k;
       w.return_value = 0;
+      w.ordered = 1;
       w.out_values = nullptr;
       w.out_indices = nullptr;
       w.idx64 = 0;
@@ -549,6 +550,7 @@ extern "C" int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, 
   if (pl.warp_rows) {
     pl.wprm.x = static_cast<const char*>(x);
     pl.wprm.return_value = return_value;
+    pl.wprm.ordered = sorted_index == DS_TOPK_SORT_INDEX ? 1 : 0;
     pl.wprm.out_values = return_value ? out_values : nullptr;
     pl.wprm.out_indices = out_indices;
     pl.wprm.idx64 = idx64;

@@ -76,6 +76,7 @@ struct WrParams {
   int32_t depth;          // chunks of the streaming ring (2 or 3)
   int32_t k;
   int32_t return_value;
+  int32_t ordered;        // outputs in ascending index order (sorted_index 1)
   void* out_values;
   void* out_indices;      // int32 or int64 (idx64)
   int32_t idx64;
@@ -541,9 +542,11 @@ struct WarpRow {
     }
   }
 
-  // ---- C: the ordered output pass --------------------------------------------------
+  // ---- C: the output pass ----------------------------------------------------------
   // Every candidate with key > kth, and the first `need` with key == kth in index
-  // order, written at consecutive positions of the row's output (ascending index).
+  // order. Ordered output: one pass, positions in ascending index order. Any
+  // other order: the keys above kth with one ballot per 32 candidates, then the
+  // ties in a short pass that stops once `need` of them are written.
   template <bool IDX64, bool RETV>
   __device__ __forceinline__ void write_out(int64_t row, int n, uint32_t kth, uint32_t need) const {
     using VT = typename std::conditional<ES == 2, uint16_t, uint32_t>::type;
@@ -551,6 +554,41 @@ struct WarpRow {
     int32_t* oi32 = static_cast<int32_t*>(p.out_indices) + obase;
     int64_t* oi64 = static_cast<int64_t*>(p.out_indices) + obase;
     VT* ov = RETV ? static_cast<VT*>(p.out_values) + obase : nullptr;
+    auto put = [&](int o, uint32_t w, int j) {
+      const int idx = ES == 2 ? static_cast<int>(w >> 16) : static_cast<int>(ci[j]);
+      if (IDX64) oi64[o] = idx;
+      else oi32[o] = idx;
+      if (RETV) ov[o] = static_cast<VT>(ES == 2 ? (w & 0xFFFFu) : w);
+    };
+    if (!p.ordered) {
+      int o_gt = 0;
+      for (int j0 = 0; j0 < n; j0 += 32 * kSelU) {
+        uint32_t wv[kSelU];
+#pragma unroll
+        for (int u = 0; u < kSelU; ++u) {
+          const int j = j0 + 32 * u + lane;
+          wv[u] = j < n ? cw[j] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kSelU; ++u) {
+          const bool sel = j0 + 32 * u + lane < n && key_of<ES>(ES == 2 ? (wv[u] & 0xFFFFu) : wv[u]) > kth;
+          const uint32_t sb = __ballot_sync(kFull, sel);
+          if (sel) put(o_gt + __popc(sb & lt), wv[u], j0 + 32 * u + lane);
+          o_gt += __popc(sb);
+        }
+      }
+      int t_eq = 0;
+      for (int j0 = 0; j0 < n && t_eq < static_cast<int>(need); j0 += 32) {
+        const int j = j0 + lane;
+        const uint32_t w = j < n ? cw[j] : 0u;
+        const bool eq = j < n && key_of<ES>(ES == 2 ? (w & 0xFFFFu) : w) == kth;
+        const uint32_t eb = __ballot_sync(kFull, eq);
+        const int r = t_eq + __popc(eb & lt);
+        if (eq && r < static_cast<int>(need)) put(o_gt + r, w, j);
+        t_eq += __popc(eb);
+      }
+      return;
+    }
     int taken_eq = 0, out = 0;
     for (int j0 = 0; j0 < n && out < p.k; j0 += 32 * kSelU) {
       uint32_t wv[kSelU], gtb[kSelU], eqb[kSelU];
@@ -574,12 +612,7 @@ struct WarpRow {
         taken_eq += __popc(eqb[u]);
         const uint32_t sb = __ballot_sync(kFull, sel);
         const int o = out + __popc(sb & lt);
-        if (sel && o < p.k) {
-          const int idx = ES == 2 ? static_cast<int>(wv[u] >> 16) : static_cast<int>(ci[j0 + 32 * u + lane]);
-          if (IDX64) oi64[o] = idx;
-          else oi32[o] = idx;
-          if (RETV) ov[o] = static_cast<VT>(ES == 2 ? (wv[u] & 0xFFFFu) : wv[u]);
-        }
+        if (sel && o < p.k) put(o, wv[u], j0 + 32 * u + lane);
         out += __popc(sb);
       }
     }
