@@ -24,9 +24,10 @@
 //  R  exact k-th key K* among the candidates: 256-bin histogram levels, the
 //     first over the 256 top-16-bit keys from t up (it also spots a NaN),
 //     each further level narrowing the range by 8 bits.
-//  C  one ordered pass over the candidates: keep key > K*, and keys == K*
-//     while their running count stays below the ties still needed; outputs
-//     are written in ascending index order (sorted_index costs nothing).
+//  C  output: keep key > K*, and the first keys == K* in index order until k
+//     are taken. For sorted_index 1, one ordered pass writes them in ascending
+//     index order (at no extra cost); otherwise the keys above K* go first
+//     (one ballot per 32 candidates) and a short pass adds the ties.
 //
 // A row whose guess fails is retried (sample threshold, a sample rank adapted to
 // the count seen, the exact k-th vector maximum) with direct passes over the
