@@ -1279,19 +1279,21 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           }
           return;
         }
-        for (int j = lane; j < round_up32(lc); j += 32) {
-          const bool gok = j < lc;
-          for (int q = 0; q < gv; ++q) {
-            const int64_t v = gok ? v0 + static_cast<int64_t>(wlist[j]) * gv + q : v1;
-            const bool vok = v < v1;
-            uint4 w = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
-            if (vok) w = blk(v);
+        if constexpr (!GV1) {  // granules of several vectors
+          for (int j = lane; j < round_up32(lc); j += 32) {
+            const bool gok = j < lc;
+            for (int q = 0; q < gv; ++q) {
+              const int64_t v = gok ? v0 + static_cast<int64_t>(wlist[j]) * gv + q : v1;
+              const bool vok = v < v1;
+              uint4 w = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
+              if (vok) w = blk(v);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              const uint32_t eb = elem_bits<ES>(w, e);
-              const uint32_t key = key_of<ES>(eb);
-              const int64_t idx = v * VEC + e - lead;
-              f(key, vok && idx >= 0 && idx < p.len && (key >= T_full || is_nan_bits<ES>(eb)));
+              for (int e = 0; e < VEC; ++e) {
+                const uint32_t eb = elem_bits<ES>(w, e);
+                const uint32_t key = key_of<ES>(eb);
+                const int64_t idx = v * VEC + e - lead;
+                f(key, vok && idx >= 0 && idx < p.len && (key >= T_full || is_nan_bits<ES>(eb)));
+              }
             }
           }
         }
@@ -1396,9 +1398,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       // grow from base_gt + min(base_eq, r_ties): when that is already k, this
       // warp has nothing to write.
       const bool none_here = base_gt + min(base_eq, r_ties) >= k;
-      // one vector per lane (vector v of the row, valid if vok), lanes in index order
-      auto write_vec = [&](const uint4& w, int64_t v, bool vok) {
-        uint32_t lg = 0, lq = 0;
+      // the counts of the selected elements of vector v (valid if vok) above and at K*
+      auto count_vec = [&](const uint4& w, int64_t v, bool vok, uint32_t& lg, uint32_t& lq) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
           const uint32_t eb = elem_bits<ES>(w, e);
@@ -1409,11 +1410,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
             lq += key == kstar;
           }
         }
-        uint32_t bg = base_gt + warp_excl_scan(lg);
-        uint32_t bq = base_eq + warp_excl_scan(lq);
-        base_gt += warp_sum(lg);
-        base_eq += warp_sum(lq);
-        if (lg + lq == 0) return;
+      };
+      // writes them from the lane's running positions bg (above K*) and bq (ties)
+      auto put_vec = [&](const uint4& w, int64_t v, bool vok, uint32_t& bg, uint32_t& bq) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
           const int64_t idx = v * VEC + e - lead;
@@ -1435,6 +1434,17 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           }
         }
       };
+      // one vector per lane (vector v of the row, valid if vok), lanes in index order
+      auto write_vec = [&](const uint4& w, int64_t v, bool vok) {
+        uint32_t lg = 0, lq = 0;
+        count_vec(w, v, vok, lg, lq);
+        uint32_t bg = base_gt + warp_excl_scan(lg);
+        uint32_t bq = base_eq + warp_excl_scan(lq);
+        base_gt += warp_sum(lg);
+        base_eq += warp_sum(lq);
+        if (lg + lq == 0) return;
+        put_vec(w, v, vok, bg, bq);
+      };
       if (gv == 1) {
         // 4 listed vectors in flight per lane, handled in list order; stop once
         // every later output would land at or beyond position k
@@ -1454,15 +1464,23 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           if (base_gt + min(base_eq, r_ties) >= k) break;
         }
       } else {
+        // one granule of gv vectors per lane: its counts first, so that positions
+        // follow index order (granule by granule, then vector by vector)
         for (int j0 = 0; j0 < (none_here ? 0 : lc); j0 += 32) {
           const int j = j0 + lane;
-          const bool gok = j < lc;
-          for (int q = 0; q < gv; ++q) {
-            const int64_t v = gok ? v0 + static_cast<int64_t>(wlist[j]) * gv + q : v1;
-            uint4 w = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
-            if (v < v1) w = blk(v);
-            write_vec(w, v, v < v1);
+          const int64_t vb = j < lc ? v0 + static_cast<int64_t>(wlist[j]) * gv : v1;
+          uint32_t lg = 0, lq = 0;
+          for (int q = 0; q < gv; ++q)
+            if (vb + q < v1) count_vec(blk(vb + q), vb + q, true, lg, lq);
+          uint32_t bg = base_gt + warp_excl_scan(lg);
+          uint32_t bq = base_eq + warp_excl_scan(lq);
+          base_gt += warp_sum(lg);
+          base_eq += warp_sum(lq);
+          if (lg + lq != 0) {
+            for (int q = 0; q < gv; ++q)
+              if (vb + q < v1) put_vec(blk(vb + q), vb + q, true, bg, bq);
           }
+          if (base_gt + min(base_eq, r_ties) >= k) break;  // warp-uniform
         }
       }
     }
