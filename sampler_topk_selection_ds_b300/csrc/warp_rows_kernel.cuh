@@ -10,8 +10,9 @@
 //
 //  T  threshold t (an order key): the warp's previous row's k-th key lowered by
 //     a margin, or, for a warp's first row, a value read off a sample of vector
-//     maxima (16 evenly spaced blocks of 32 vectors). t is only a guess; the
-//     step below checks it.
+//     maxima (16 evenly spaced blocks of 32 vectors), or of the elements of
+//     those vectors when k is over a quarter of the row's vectors. t is only a
+//     guess; the step below checks it.
 //  S  stream the row once through a per-warp shared-memory ring of 2 KB bulk
 //     async copies. In each chunk lane j owns 4 consecutive 16-byte vectors
 //     (64 contiguous bytes); it marks its elements >= t (or NaN) in one 32-bit
@@ -30,7 +31,8 @@
 //     (one ballot per 32 candidates) and a short pass adds the ties.
 //
 // A row whose guess fails is retried (sample threshold, a sample rank adapted to
-// the count seen, the exact k-th vector maximum) with direct passes over the
+// the count seen, the exact k-th vector maximum, or for dense rows the exact top
+// 16 key bits of the k-th element) with direct passes over the
 // row; a row that still fails (massive ties, a NaN, k above the number of
 // finite vectors) takes the exact fallback: 8-bit radix levels over every
 // element of the row, then one ordered output pass. Rows with a NaN set the
@@ -319,7 +321,8 @@ struct WarpRow {
   // are sampled in 16 evenly spaced blocks of 32 consecutive vectors (coalesced,
   // 1/8 of a 64 KB row's cache lines, which the stream then finds in L2), and the
   // threshold is the q-th largest sampled maximum, q about 1.2 k times the
-  // sampled fraction plus a margin: a guess that the stream verifies.
+  // sampled fraction plus a margin: a guess that the stream verifies. Dense rows
+  // rank the sampled elements with the same q (the sampled fraction is the same).
   __device__ __forceinline__ int sample_size(const Geo& g) const {
     return g.nv <= 32 * kWrSampleBlocks ? g.nv : 32 * kWrSampleBlocks;
   }
@@ -336,12 +339,51 @@ struct WarpRow {
     else r = static_cast<uint32_t>(static_cast<int64_t>(q) * (5 * p.k / 4) / (n > 0 ? n : 1)) + 4;
     return r < 1u ? 1u : r;
   }
+  // Dense rows, where k is over a quarter of the row's vectors, rank element keys
+  // instead: with several selected elements per vector, the count of elements
+  // above the q-th largest vector maximum is no longer close to q.
+  __device__ __forceinline__ bool dense(const Geo& g) const { return 4 * p.k > g.nv; }
+
+  // The q-th largest top-16 key bits among the elements of the vectors
+  // i * vstride + lane (i < steps, vectors past the row skipped): two 8-bit
+  // histogram levels, each over the vectors read again (from L1 or L2).
+  __device__ uint32_t elem_threshold(const Geo& g, uint32_t q, int steps, int vstride) const {
+    uint32_t b1 = 0, need = q;
+    for (int level = 0; level < 2; ++level) {
+      wr_clear_hist(hist);
+      for (int i = 0; i < steps; ++i) {
+        const int v = i * vstride + lane;
+        if (v >= g.nv) continue;
+        const uint4 w = load(g, v);  // elements outside the row read as -inf
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const uint32_t kk = key_of<ES>(elem_bits<ES>(w, e)) >> (KB - 16);
+          if (level == 0) atomicAdd(&hist[kk >> 8], 1u);
+          else if ((kk >> 8) == b1) atomicAdd(&hist[kk & 0xFFu], 1u);
+        }
+      }
+      __syncwarp();
+      uint32_t above, cnt;
+      const uint32_t b = wr_find_bin(hist, need, &above, &cnt);
+      __syncwarp();
+      need -= above;
+      b1 = level == 0 ? b : ((b1 << 8) | b);
+    }
+    uint32_t t = b1;
+    if constexpr (ES == 4) t <<= 16;
+    return t < wr_key_floor<ES>() ? wr_key_floor<ES>() : t;
+  }
+
   __device__ uint32_t sample_threshold(const Geo& g, uint32_t q) const {
     const int nvec = g.nv;
     constexpr int kPer = kWrSampleBlocks;  // vectors per lane
     const bool whole = nvec <= 32 * kPer;
     const int ns = whole ? nvec : 32 * kPer;
     const int bstride = whole ? 32 : (nvec - 32) / (kPer - 1);  // block starts: i * bstride
+    if (dense(g)) {  // q ranks the sampled elements, VEC per sampled vector
+      if (q > static_cast<uint32_t>(ns * VEC)) return wr_key_floor<ES>();
+      return elem_threshold(g, q, kPer, bstride);
+    }
     if (q > static_cast<uint32_t>(ns)) return wr_key_floor<ES>();
     uint32_t kk[kPer];
 #pragma unroll
@@ -697,6 +739,7 @@ struct WarpRow {
   // Two passes over the row, one histogram update per vector. At least k
   // elements reach the result, so it is a threshold that always holds.
   __device__ uint32_t vecmax_threshold(const Geo& g) const {
+    if (dense(g)) return elem_threshold(g, static_cast<uint32_t>(p.k), (g.nv + 31) / 32, 32);
     if (g.nv < p.k) return wr_key_floor<ES>();
     const int nsteps = (g.nv + 31) / 32;
     uint32_t need = static_cast<uint32_t>(p.k), b1 = 0;

@@ -189,3 +189,26 @@ def test_warp_rows_off_boundary_nan_and_causal_tail():
     gv, gi, gf = run_view(view, 512, sorted_index=False, return_value=True)
     assert gf & 1
     assert_parity(x, 512, False, True, gpu_out=(gv, gi, gf))
+
+
+@pytest.mark.parametrize("dtype,length,ks", [
+    (torch.bfloat16, 2048, [300, 600, 1024]),    # read whole: the exact k-th element's key
+    (torch.bfloat16, 4100, [256, 512, 1000]),    # read whole, ragged
+    (torch.bfloat16, 8192, [512, 1024]),         # sampled elements
+    (torch.float32, 2304, [300, 512]),           # sampled elements, top 16 key bits
+])
+def test_warp_rows_dense_k(dtype, length, ks):
+    """k over a quarter of the row's 16-byte vectors: thresholds from element
+    keys. Ordinary rows, rows of few distinct values (ties at the k-th key
+    beyond the candidate room: the exact fallback), and rows whose scale
+    changes from one row to the next (the carried threshold fails)."""
+    b = _wr_batch(length)
+    x = workloads.random_rows(b, length, dtype, 7300 + length, style="normal")
+    ties = workloads.random_rows(b, length, dtype, 7301 + length, style="ties")
+    x[1::7] = ties[1::7]
+    f = x.float()
+    scale = 1.0 + (torch.arange(b) % 4).float()[:, None] * 3.0
+    x = torch.where(torch.isfinite(f), f * scale, f).to(dtype).contiguous()
+    for k in ks:
+        _assert_path(x, k)
+        assert_parity(x, k, sorted_index=(k % 2 == 0), return_value=True)
