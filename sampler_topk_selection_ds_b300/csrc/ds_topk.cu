@@ -463,10 +463,34 @@ cudaError_t launch_dtype(const Plan& pl, cudaStream_t stream) {
 
 bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
 
+// Rows per SM from which the value order sorts one row per warp (measured: with
+// 4 rows per SM the CTA sort is still as fast, from 8 on the warp sort is faster).
+#ifndef DS_TOPK_VO_WARP_ROWS_PER_SM
+#define DS_TOPK_VO_WARP_ROWS_PER_SM 8
+#endif
+
+template <int E>
+cudaError_t launch_vo_warp(cudaLaunchConfig_t cfg, const ds_topk_dev::OrderParams& op, int sm_count) {
+  constexpr int warps = ds_topk_dev::kVoWarps;
+  const int64_t ctas = (op.batch + warps - 1) / warps;
+  const int64_t max_ctas = static_cast<int64_t>(sm_count) * 16;  // rows are walked with a grid stride
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas < max_ctas ? ctas : max_ctas), 1, 1);
+  cfg.blockDim = dim3(32 * warps, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  using namespace ds_topk_dev;
+  if (op.idx64)
+    return op.return_value ? cudaLaunchKernelEx(&cfg, topk_value_order_warp_kernel<E, true, true>, op)
+                           : cudaLaunchKernelEx(&cfg, topk_value_order_warp_kernel<E, true, false>, op);
+  return op.return_value ? cudaLaunchKernelEx(&cfg, topk_value_order_warp_kernel<E, false, true>, op)
+                         : cudaLaunchKernelEx(&cfg, topk_value_order_warp_kernel<E, false, false>, op);
+}
+
 // sorted_index == DS_TOPK_SORT_VALUE: a second kernel on the same stream sorts
-// each row's k outputs by value (one CTA per row, a bitonic sort in shared
-// memory). It starts early through programmatic dependent launch and waits for
-// the selection kernel's outputs before reading them.
+// each row's k outputs by value: for many bf16 rows of at most 65536 elements
+// and k <= 1024 one warp per row with the sort words in registers, otherwise one
+// CTA per row with a bitonic sort in shared memory. It starts early through
+// programmatic dependent launch and waits for the selection kernel's outputs
+// before reading them.
 template <int ES>
 cudaError_t launch_value_order(const char* x, int64_t batch, int64_t len, int64_t row_stride_bytes, int k,
                                int return_value, void* out_values, void* out_indices, int idx64,
@@ -484,18 +508,33 @@ cudaError_t launch_value_order(const char* x, int64_t batch, int64_t len, int64_
   op.out_values = return_value ? out_values : nullptr;
   op.out_indices = out_indices;
   op.idx64 = idx64;
-  const int threads = n2 / 2 < 1024 ? n2 / 2 : 1024;  // n2 >= 64: at least one warp
-  const int64_t max_grid = static_cast<int64_t>(sm_count) * 16;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(batch < max_grid ? batch : max_grid), 1, 1);
-  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(n2) * 8;  // <= 32 KB
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (ES == 2 && len <= ds_topk_dev::kVoMaxLen && k <= ds_topk_dev::kVoMaxK &&
+      batch >= static_cast<int64_t>(sm_count) * DS_TOPK_VO_WARP_ROWS_PER_SM) {
+    // one warp per row, 32-bit sort words in registers; with fewer rows one CTA
+    // per row finishes sooner, its warps sharing each row's sort
+    int n32 = 32;
+    while (n32 < k) n32 <<= 1;
+    switch (n32 / 32) {
+      case 1: return launch_vo_warp<1>(cfg, op, sm_count);
+      case 2: return launch_vo_warp<2>(cfg, op, sm_count);
+      case 4: return launch_vo_warp<4>(cfg, op, sm_count);
+      case 8: return launch_vo_warp<8>(cfg, op, sm_count);
+      case 16: return launch_vo_warp<16>(cfg, op, sm_count);
+      default: return launch_vo_warp<32>(cfg, op, sm_count);
+    }
+  }
+  const int threads = n2 / 2 < 1024 ? n2 / 2 : 1024;  // n2 >= 64: at least one warp
+  const int64_t max_grid = static_cast<int64_t>(sm_count) * 16;
+  cfg.gridDim = dim3(static_cast<unsigned>(batch < max_grid ? batch : max_grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(n2) * 8;  // <= 32 KB
   return cudaLaunchKernelEx(&cfg, ds_topk_dev::topk_value_order_kernel<ES>, op);
 }
 

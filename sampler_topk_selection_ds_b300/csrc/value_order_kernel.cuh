@@ -1,12 +1,14 @@
 // value_order_kernel.cuh — optional output order by value (sorted_index = 2).
 //
-// The selection kernels write each row's k outputs in ascending index order.
-// For value order, this kernel runs after them on the same stream: one CTA per
-// row reads the k selected elements (from the values the selection wrote, or
-// gathered from x when no values are returned), forms 64-bit sort words (order
-// key << 32 | ~index) and sorts them descending with a bitonic network (k <=
-// 4096: at most 32 KB of shared memory); strides below 64 run in registers with
-// warp shuffles, so only the wider ones pay a CTA barrier.
+// For value order, a sort kernel runs after the selection on the same stream and
+// reorders each row's k outputs in place. It reads the k selected elements (from
+// the values the selection wrote, or gathered from x when no values are
+// returned) as sort words and sorts them descending with a bitonic network:
+//  - one CTA per row (any k <= 4096): 64-bit words (order key << 32 | ~index) in
+//    at most 32 KB of shared memory; strides below 64 run in registers with warp
+//    shuffles, so only the wider ones pay a CTA barrier;
+//  - one warp per row (many bf16 rows of at most 65536 elements, k <= 1024):
+//    32-bit words (16-bit key << 16 | ~16-bit index) in registers.
 // Descending words give value descending, and equal values by ascending index
 // (the complement of the index sorts the lower index first), which is the
 // selection's own total order; every word is distinct, so no stability is
@@ -146,6 +148,142 @@ __global__ void __launch_bounds__(1024) topk_value_order_kernel(const OrderParam
       }
     }
     __syncthreads();  // the next row reuses sw
+  }
+}
+
+}  // namespace ds_topk_dev
+
+namespace ds_topk_dev {
+
+// ---- one warp per row: bf16 rows of at most 65536 elements, k <= 1024 ----------------
+// A sort word is 32 bits, the 16-bit order key above the complemented 16-bit
+// index, so descending words are value descending, equal values by ascending
+// index. Lane l holds E = n2 / 32 of them in registers (n2 = k rounded up to a
+// power of two, at least 32) and no CTA barrier is involved, so a CTA sorts
+// several rows at once. (With 64-bit words, as fp32 keys need, the register
+// sort costs more than the CTA sort above, which those rows keep.)
+// Input word j is read by lane j mod 32 (coalesced) into sort position
+// (j mod 32) E + j / 32: where a word starts does not change the sorted result.
+// The sorted words go out through a per-warp shared-memory stage, written at the
+// lane's sort positions and read back at output position j = e 32 + lane, with one
+// pad word after every 32 so that both sides are free of bank conflicts.
+constexpr int kVoMaxK = 1024;
+constexpr int kVoMaxLen = 65536;
+constexpr int kVoWarps = 8;
+
+// Descending bitonic sort of the 32 E words of a warp, word e of lane l at sort
+// position i = l E + e, in the form where every comparator points the same way:
+// for each block size 2, 4, .., 32 E, position i of a block first pairs with its
+// mirror i ^ (size - 1), then (half-cleaners) with i ^ stride for stride = size /
+// 4, .., 1; the lower position of a pair keeps the larger word. Pairs inside a
+// lane (stride < E) are compile-time (one max, one min); wider ones exchange
+// through shuffles, the lane's role (lower or upper) being one predicate per step.
+template <typename W>
+__device__ __forceinline__ W vo_max(W a, W b) { return a > b ? a : b; }
+template <typename W>
+__device__ __forceinline__ W vo_min(W a, W b) { return a > b ? b : a; }
+// The larger of a and the partner's word b if `larger`, else the smaller: one
+// compare folded with the predicate, one select.
+template <typename W>
+__device__ __forceinline__ W vo_keep(W a, W b, bool larger) { return (a > b) == larger ? a : b; }
+
+template <typename W, int E>
+__device__ __forceinline__ void vo_sort_desc(W (&x)[E], int lane) {
+  constexpr int N = 32 * E;
+#pragma unroll
+  for (int size = 2; size <= N; size <<= 1) {
+    if (size <= E) {  // mirror pairs inside the lane
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if ((e & (size >> 1)) == 0) {
+          const int f = e ^ (size - 1);
+          const W a = x[e], b = x[f];
+          x[e] = vo_max(a, b);
+          x[f] = vo_min(a, b);
+        }
+      }
+    } else {  // the mirror of word e sits in lane l ^ m as word E - 1 - e
+      const int m = (size - 1) / E;
+      const bool lower = (lane & ((size >> 1) / E)) == 0;
+#pragma unroll
+      for (int e = 0; e < E / 2; ++e) {
+        const W ya = __shfl_xor_sync(0xFFFFFFFFu, x[E - 1 - e], m);
+        const W yb = __shfl_xor_sync(0xFFFFFFFFu, x[e], m);
+        x[e] = vo_keep(x[e], ya, lower);
+        x[E - 1 - e] = vo_keep(x[E - 1 - e], yb, lower);
+      }
+      if (E == 1) x[0] = vo_keep(x[0], __shfl_xor_sync(0xFFFFFFFFu, x[0], m), lower);
+    }
+#pragma unroll
+    for (int stride = size >> 2; stride > 0; stride >>= 1) {
+      if (stride < E) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if ((e & stride) == 0) {
+            const W a = x[e], b = x[e | stride];
+            x[e] = vo_max(a, b);
+            x[e | stride] = vo_min(a, b);
+          }
+        }
+      } else {
+        const int d = stride / E;
+        const bool lower = (lane & d) == 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          x[e] = vo_keep(x[e], __shfl_xor_sync(0xFFFFFFFFu, x[e], d), lower);
+        }
+      }
+    }
+  }
+}
+
+template <int E, bool IDX64, bool RETV>
+__global__ void __launch_bounds__(32 * kVoWarps) topk_value_order_warp_kernel(const OrderParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the selection's outputs
+  constexpr int N = 32 * E;
+  __shared__ uint32_t stage[kVoWarps][N + N / 32];
+  const int lane = threadIdx.x & 31;
+  uint32_t* st = stage[threadIdx.x >> 5];
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kVoWarps;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kVoWarps + (threadIdx.x >> 5); row < p.batch; row += nw) {
+    const char* rowp = p.x + row * p.row_stride_bytes;
+    const int64_t ob = row * static_cast<int64_t>(p.k);
+    uint16_t* ov = RETV ? static_cast<uint16_t*>(p.out_values) + ob : nullptr;
+    uint32_t x[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int j = e * 32 + lane;
+      uint32_t w = 0u;  // padding sorts last
+      if (j < p.k) {
+        int64_t idx = get_index(p.out_indices, ob + j, IDX64);
+        if (idx < 0 || idx >= p.len) idx = 0;  // never read outside the row
+        const uint32_t bits = RETV ? static_cast<uint32_t>(ov[j]) : load_bits<2>(rowp, idx);
+        w = (key_of<2>(bits) << 16) | (0xFFFFu - static_cast<uint32_t>(idx));
+      }
+      x[e] = w;
+    }
+    vo_sort_desc<uint32_t, E>(x, lane);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = lane * E + e;
+      st[i + i / 32] = x[e];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int j = e * 32 + lane;
+      if (j < p.k) {
+        const uint32_t w = st[j + j / 32];
+        const uint32_t idx = 0xFFFFu - (w & 0xFFFFu);
+        put_index(p.out_indices, ob + j, idx, IDX64);
+        if constexpr (RETV) {
+          uint32_t bits;
+          if (!bits_of_key<2>(w >> 16, &bits)) bits = load_bits<2>(rowp, idx);
+          ov[j] = static_cast<uint16_t>(bits);
+        }
+      }
+    }
+    __syncwarp();  // the next row rewrites the stage
   }
 }
 

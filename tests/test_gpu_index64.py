@@ -39,3 +39,5 @@ def test_int64_indices_every_path(dtype, order):
     check_i64(workloads.random_rows(8, 4096, dtype, 71, style="ties"), 300, order)        # CTA per row
     check_i64(workloads.random_rows(2, 300000, dtype, 72, style="normal"), 4096, order)   # cluster
     check_i64(workloads.random_rows(4 * sms + 3, 1000, dtype, 73, style="normal"), 64, order)  # warp rows
+    # many rows: for bf16 and value order also the one-warp-per-row sort
+    check_i64(workloads.random_rows(8 * sms + 3, 1000, dtype, 74, style="ties"), 300, order)

@@ -90,3 +90,26 @@ def test_value_order_nan_rows_in_range():
     x = workloads.random_rows(6, 5000, torch.bfloat16, 616, style="normal")
     x[2, 17] = float("nan")
     check_value_order(x, 300)  # the NaN row is only checked for the flag and in-range indices
+
+
+ALL_WIDTHS = (1, 2, 31, 32, 33, 64, 65, 100, 128, 129, 256, 257, 300, 511, 512, 513, 1000, 1024, 1025)
+
+
+@pytest.mark.parametrize("dtype,n,ks", [(torch.bfloat16, 3000, ALL_WIDTHS),
+                                        (torch.bfloat16, 65536, (1, 33, 512, 1024)),
+                                        (torch.bfloat16, 70001, (1, 33, 512, 1024)),
+                                        (torch.float32, 3000, (1, 33, 512, 1024, 1025))])
+def test_value_order_register_sort_widths(dtype, n, ks):
+    """Many bf16 rows of at most 65536 elements with k <= 1024 sort one row per
+    warp in registers, n2 / 32 words per lane for n2 = k rounded up to a power of
+    two (at least 32): every width from 1 to 32 words, and the k just above 1024
+    that goes back to the CTA sort. 32-bit sort words hold a 16-bit index, so the
+    last index of a 65536-element row complements to 0. Longer bf16 rows and fp32
+    rows keep the CTA sort with 64-bit words. Ties and signed zeros throughout."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    b = 8 * sms + 3 if dtype == torch.bfloat16 and n <= 65536 else 40  # the warp sort needs 8 rows per SM
+    x = workloads.random_rows(b, n, dtype, 617 + n, style="signed_zero")
+    x[1::2] = workloads.random_rows(b, n, dtype, 618 + n, style="ties")[1::2]
+    x[5, n - 1] = 3e38  # a ties row's largest element at its last index
+    for k in ks:
+        check_value_order(x, k, return_value=(k % 2 == 0))
