@@ -426,6 +426,7 @@ constexpr int kXpreEq = 7;    // [7]      cluster: '==' elements of lower ranks 
 constexpr int kOvw = 8;       // [8..11]  overflow words of cluster levels (local + 3 received)
 constexpr int kOvl = 12;      // [12]     overflow word of local levels
 constexpr int kRdTot = 13;    // [13]     fallback: listed granules of the whole row
+constexpr int kRdMax = 14;    // [14]     fallback: most listed granules of one warp
 constexpr int kWtot = 16;     // [16..31] per-warp totals (2 x kWarps)
 constexpr int kSegBase = 32;  // [32..39] candidate segment start per warp
 constexpr int kSegCnt = 40;   // [40..47] candidate segment length per warp
@@ -1201,12 +1202,13 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       }
       __syncthreads();
       if (warp == 0) {
-        uint32_t c[4], sum = 0;
+        uint32_t c[4], sum = 0, most = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int q = lane * 4 + i;
           c[i] = q < G ? gcnt[q] : 0u;
           sum += c[i];
+          most = max(most, c[i]);
         }
         uint32_t run = warp_excl_scan(sum);
 #pragma unroll
@@ -1215,12 +1217,19 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           if (q < G) gpre[q] = run;
           run += c[i];
         }
+        most = __reduce_max_sync(kFull, most);
         if (lane == 31) misc[kRdTot] = run;
+        if (lane == 0) misc[kRdMax] = most;
       }
       __syncthreads();
       const uint32_t rd_total = misc[kRdTot];
+      const uint32_t rd_share = (rd_total + G - 1) / G;
       const int rd_cap = static_cast<int>(union_bytes(p.g_cap_pad, p.cand_cap) / 4 / kWarps);
-      const bool rd = gv == 1 && G > 1 && (rd_total + G - 1) / G <= static_cast<uint32_t>(rd_cap);  // cluster-uniform
+      // spread only lists that are skewed (a warp holds over twice its share):
+      // even lists (rows of a few levels spread over the whole row) gain nothing
+      // from it but its cost; cluster-uniform
+      const bool rd = gv == 1 && G > 1 && misc[kRdMax] > 2u * rd_share + 32u &&
+                      rd_share <= static_cast<uint32_t>(rd_cap);
       uint32_t* ra = reinterpret_cast<uint32_t*>(uni) + warp * rd_cap;  // this warp's share: row vector indices
       int rn = 0;
       if (rd) {
@@ -1364,12 +1373,65 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
         }
       }
       const uint32_t r_ties = need;
+      // Per vector, the row elements above K* (mg) and equal to it (mq) as bit
+      // masks; every such element also reaches the threshold t. Elements outside
+      // the row read as -inf, which can equal K*, so partly covered blocks are
+      // masked to the row.
+      auto kstar_masks = [&](const uint4& w, int64_t v, bool vok, uint32_t& mg, uint32_t& mq) {
+        mg = 0u;
+        mq = 0u;
+        if (!vok) return;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const uint32_t key = key_of<ES>(elem_bits<ES>(w, e));
+          mg |= static_cast<uint32_t>(key > kstar) << e;
+          mq |= static_cast<uint32_t>(key == kstar) << e;
+        }
+        const int64_t e0 = v * VEC - lead;  // row index of the block's element 0
+        if (e0 < 0 || e0 + VEC > p.len) {
+          uint32_t inrow = 0u;
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) inrow |= static_cast<uint32_t>(e0 + e >= 0 && e0 + e < p.len) << e;
+          mg &= inrow;
+          mq &= inrow;
+        }
+      };
+      // The listed vectors of this warp, g(w, v, vok) for each, in list order.
+      auto visit_vecs = [&](auto&& g) {
+        if (gv == 1) {
+          constexpr int UV = 4;
+          for (int jb = 0; jb < lcnt; jb += 32 * UV) {
+            uint4 w[UV];
+            int64_t v[UV];
+#pragma unroll
+            for (int u = 0; u < UV; ++u) {
+              const int j = jb + 32 * u + lane;
+              v[u] = j < lcnt ? static_cast<int64_t>(vec_at(j)) : -1;
+              w[u] = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
+              if (v[u] >= 0) w[u] = blk(v[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < UV; ++u) g(w[u], v[u], v[u] >= 0);
+          }
+          return;
+        }
+        if constexpr (!GV1) {
+          for (int j = lane; j < lc; j += 32)
+            for (int q = 0; q < gv; ++q) {
+              const int64_t v = v0 + static_cast<int64_t>(wlist[j]) * gv + q;
+              if (v < v1) g(blk(v), v, true);
+            }
+        }
+      };
       // counts of this warp's list, then prefixes over warps and cluster CTAs
-      uint32_t c_gt = 0, c_eq = 0;
-      visit([&](uint32_t key, bool ok) {
-        c_gt += __popc(__ballot_sync(kFull, ok && key > kstar));
-        c_eq += __popc(__ballot_sync(kFull, ok && key == kstar));
+      uint32_t l_gt = 0, l_eq = 0;
+      visit_vecs([&](const uint4& w, int64_t v, bool vok) {
+        uint32_t mg, mq;
+        kstar_masks(w, v, vok, mg, mq);
+        l_gt += __popc(mg);
+        l_eq += __popc(mq);
       });
+      const uint32_t c_gt = warp_sum(l_gt), c_eq = warp_sum(l_eq);
       if (lane == 0) {
         wtot[warp] = c_gt;
         wtot[kWarps + warp] = c_eq;
@@ -1398,56 +1460,31 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       // grow from base_gt + min(base_eq, r_ties): when that is already k, this
       // warp has nothing to write.
       const bool none_here = base_gt + min(base_eq, r_ties) >= k;
-      // the counts of the selected elements of vector v (valid if vok) above and at K*
-      auto count_vec = [&](const uint4& w, int64_t v, bool vok, uint32_t& lg, uint32_t& lq) {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          const uint32_t eb = elem_bits<ES>(w, e);
-          const uint32_t key = key_of<ES>(eb);
-          const int64_t ix = v * VEC + e - lead;
-          if (vok && ix >= 0 && ix < p.len && (key >= T_full || is_nan_bits<ES>(eb))) {
-            lg += key > kstar;
-            lq += key == kstar;
+      // writes the elements of masks mg / mq of vector v in index order, from the
+      // lane's running positions bg (above K*) and bq (ties)
+      auto put_masked = [&](const uint4& w, int64_t v, uint32_t mg, uint32_t mq, uint32_t& bg, uint32_t& bq) {
+        const int64_t e0 = v * VEC - lead;
+        uint32_t m = mg | mq;
+        while (m) {
+          const int e = __ffs(m) - 1;
+          m &= m - 1u;
+          uint32_t pos = 0xFFFFFFFFu;
+          if ((mg >> e) & 1u) {
+            pos = bg + min(bq, r_ties);
+            ++bg;
+          } else {
+            if (bq < r_ties) pos = bg + bq;
+            ++bq;
+          }
+          if (pos < k) {
+            put_index(p.out_indices, out_base + pos, e0 + e, p.idx64);
+            if (out_val) out_val[pos] = static_cast<VT>(elem_bits<ES>(w, e));
           }
         }
-      };
-      // writes them from the lane's running positions bg (above K*) and bq (ties)
-      auto put_vec = [&](const uint4& w, int64_t v, bool vok, uint32_t& bg, uint32_t& bq) {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          const int64_t idx = v * VEC + e - lead;
-          const uint32_t bits = elem_bits<ES>(w, e);
-          const uint32_t key = key_of<ES>(bits);
-          if (vok && idx >= 0 && idx < p.len && (key >= T_full || is_nan_bits<ES>(bits))) {
-            uint32_t pos = 0xFFFFFFFFu;
-            if (key > kstar) {
-              pos = bg + min(bq, r_ties);
-              ++bg;
-            } else if (key == kstar) {
-              if (bq < r_ties) pos = bg + bq;
-              ++bq;
-            }
-            if (pos < k) {
-              put_index(p.out_indices, out_base + pos, idx, p.idx64);
-              if (out_val) out_val[pos] = static_cast<VT>(bits);
-            }
-          }
-        }
-      };
-      // one vector per lane (vector v of the row, valid if vok), lanes in index order
-      auto write_vec = [&](const uint4& w, int64_t v, bool vok) {
-        uint32_t lg = 0, lq = 0;
-        count_vec(w, v, vok, lg, lq);
-        uint32_t bg = base_gt + warp_excl_scan(lg);
-        uint32_t bq = base_eq + warp_excl_scan(lq);
-        base_gt += warp_sum(lg);
-        base_eq += warp_sum(lq);
-        if (lg + lq == 0) return;
-        put_vec(w, v, vok, bg, bq);
       };
       if (gv == 1) {
-        // 4 listed vectors in flight per lane, handled in list order; stop once
-        // every later output would land at or beyond position k
+        // 4 listed vectors in flight per lane, one vector per lane at a time, in
+        // list order; stop once every later output would land at or beyond k
         constexpr int UV = 4;
         for (int jb = 0; jb < (none_here ? 0 : lcnt); jb += 32 * UV) {
           uint4 w[UV];
@@ -1460,7 +1497,16 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
             if (v[u] >= 0) w[u] = blk(v[u]);
           }
 #pragma unroll
-          for (int u = 0; u < UV; ++u) write_vec(w[u], v[u], v[u] >= 0);
+          for (int u = 0; u < UV; ++u) {
+            uint32_t mg, mq;
+            kstar_masks(w[u], v[u], v[u] >= 0, mg, mq);
+            const uint32_t lg = __popc(mg), lq = __popc(mq);
+            uint32_t bg = base_gt + warp_excl_scan(lg);
+            uint32_t bq = base_eq + warp_excl_scan(lq);
+            base_gt += warp_sum(lg);
+            base_eq += warp_sum(lq);
+            put_masked(w[u], v[u], mg, mq, bg, bq);
+          }
           if (base_gt + min(base_eq, r_ties) >= k) break;
         }
       } else {
@@ -1471,14 +1517,24 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           const int64_t vb = j < lc ? v0 + static_cast<int64_t>(wlist[j]) * gv : v1;
           uint32_t lg = 0, lq = 0;
           for (int q = 0; q < gv; ++q)
-            if (vb + q < v1) count_vec(blk(vb + q), vb + q, true, lg, lq);
+            if (vb + q < v1) {
+              uint32_t mg, mq;
+              kstar_masks(blk(vb + q), vb + q, true, mg, mq);
+              lg += __popc(mg);
+              lq += __popc(mq);
+            }
           uint32_t bg = base_gt + warp_excl_scan(lg);
           uint32_t bq = base_eq + warp_excl_scan(lq);
           base_gt += warp_sum(lg);
           base_eq += warp_sum(lq);
           if (lg + lq != 0) {
             for (int q = 0; q < gv; ++q)
-              if (vb + q < v1) put_vec(blk(vb + q), vb + q, true, bg, bq);
+              if (vb + q < v1) {
+                const uint4 w = blk(vb + q);
+                uint32_t mg, mq;
+                kstar_masks(w, vb + q, true, mg, mq);
+                put_masked(w, vb + q, mg, mq, bg, bq);
+              }
           }
           if (base_gt + min(base_eq, r_ties) >= k) break;  // warp-uniform
         }
