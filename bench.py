@@ -16,7 +16,10 @@ The line's headline is the decode-shaped bf16 indexer call (16384 rows of 32768,
 k=512), the largest single-GPU workload. The other workloads (fp32 sampler,
 bf16 indexer prefill, adversarial rows, the small fp32 case) ride along in the
 same line under "per_workload", each timed over at least --min-ms of device
-work, with its own roofline fraction and CPU-oracle baseline.
+work, with its own roofline fraction and CPU-oracle baseline. Each workload that
+fits in L2 also gets an "l2_hot" figure (every step on one input copy; labelled,
+never the headline), and each a "torch_topk" figure: torch.topk on the same
+input, as context for the speed-ups the method's pages quote, not as a baseline.
 
 The metric is the pages' own: effective memory bandwidth, (input bytes read +
 output bytes written) / time, because TopK does no floating-point math
@@ -404,18 +407,75 @@ class Bench:
                 self.step(i, self.stream)
         self.stream.synchronize()
 
-    def graph(self, n):
-        """A CUDA graph of n steps (starting at copy 0), replayed once before use
-        so that no timed replay is a graph's first."""
-        if n not in self.graphs:
+    def graph(self, n, hot=False):
+        """A CUDA graph of n steps (starting at copy 0; every step on copy 0 if
+        hot), replayed once before use so that no timed replay is a graph's first."""
+        if (n, hot) not in self.graphs:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=self.stream):
                 for i in range(n):
-                    self.step(i, torch.cuda.current_stream())
+                    self.step(0 if hot else i, torch.cuda.current_stream())
             g.replay()
             self.stream.synchronize()
-            self.graphs[n] = g
-        return self.graphs[n]
+            self.graphs[(n, hot)] = g
+        return self.graphs[(n, hot)]
+
+    def _time_graph(self, g, replays):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(self.dev)
+        with torch.cuda.stream(self.stream):
+            ev0.record(self.stream)
+            for _ in range(replays):
+                g.replay()
+            ev1.record(self.stream)
+        self.stream.synchronize()
+        return ev0.elapsed_time(ev1) / 1e3
+
+    def l2_hot(self, min_ms):
+        """The same step with every call on one input copy, which stays in L2
+        between calls: labelled L2-hot, beside the cold (rotating) figure. None
+        when one input alone exceeds four times L2."""
+        if self.copies == 1:
+            return None
+        n = self.chunk
+        g = self.graph(n, hot=True)
+        est = self._time_graph(g, 1) / n
+        replays = max(3, math.ceil(min_ms / 1e3 / est / n))
+        sec = self._time_graph(g, replays)
+        steps = replays * n
+        w = self.w
+        return {"steps": steps, "ms_per_step": round(sec / steps * 1e3, 6),
+                "value": round(aggregate_value(w.bytes_in + w.bytes_out, steps, 1, sec), 3), "unit": "GB/s",
+                "note": "L2-hot: every step reads the same resident input copy (not the headline figure)"}
+
+    def torch_topk_context(self, min_ms):
+        """torch.topk(x, k, sorted=False) on the same resident input, warm, in the
+        same units (this method's algorithmic bytes over its time): context for
+        the speed-ups the method's pages quote, not a baseline of the method."""
+        w, x = self.w, self.xs[0]
+        if x.stride(1) != 1 or x.stride(0) != w.length:
+            return None
+        with torch.cuda.stream(self.stream):
+            for _ in range(3):
+                torch.topk(x, w.k, dim=1, largest=True, sorted=False)
+            self.stream.synchronize()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(self.stream)
+            torch.topk(x, w.k, dim=1, largest=True, sorted=False)
+            ev1.record(self.stream)
+            self.stream.synchronize()
+            est = ev0.elapsed_time(ev1) / 1e3
+            calls = max(3, min(2000, math.ceil(min_ms / 1e3 / est)))
+            ev0.record(self.stream)
+            for _ in range(calls):
+                torch.topk(x, w.k, dim=1, largest=True, sorted=False)
+            ev1.record(self.stream)
+        self.stream.synchronize()
+        sec = ev0.elapsed_time(ev1) / 1e3
+        return {"calls": calls, "ms_per_call": round(sec / calls * 1e3, 6),
+                "value": round(aggregate_value(w.bytes_in + w.bytes_out, calls, 1, sec), 3), "unit": "GB/s",
+                "note": "context only: torch.topk(x, k, sorted=False), same input, warm (copy 0, "
+                        "so L2-hot when it fits); a library kernel, not this method"}
 
     def replay(self, steps):
         """Enqueue exactly `steps` steps (whole chunks, then the remainder)."""
@@ -478,6 +538,9 @@ def run_extra(dstk, w, dev, stream, args):
            "rows_per_s": round(w.batch * steps / sec, 1), "l2": b.l2_note,
            "roofline": b.roofline(sec, steps, w.name), "plan": b.plan.as_dict(),
            "gpu_launches": steps * b.launches}
+    if not args.no_context:
+        out["l2_hot"] = b.l2_hot(args.min_ms / 4)
+        out["torch_topk"] = b.torch_topk_context(args.min_ms / 4)
     b.free()
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, min_seconds=args.cpu_seconds / 2)
@@ -514,6 +577,10 @@ def run_ours(args, w):
     long_run = {"steps": long_steps, "ms_per_step": round(long_sec / long_steps * 1e3, 6),
                 "value": round(aggregate_value(bytes_step, long_steps, 1, long_sec), 3)}
     l2_note, plan, launches = b.l2_note, b.plan, b.launches
+    context = {}
+    if rank == 0 and not args.no_context:
+        context = {"l2_hot": b.l2_hot(args.min_ms / 4),
+                   "torch_topk": b.torch_topk_context(args.min_ms / 4) if args.order == "workload" else None}
     b.free()
 
     # end to end through the public API with host buffers (pinned), copies inside
@@ -541,6 +608,7 @@ def run_ours(args, w):
             "rows_per_s": round(w.batch * args.steps * world / max_seconds, 1),
             "roofline": roof,
             "long_run": long_run,
+            **context,
             "e2e": e2e,
             "gpu_launches": args.steps * launches,
             "plan": plan.as_dict(),
@@ -624,6 +692,8 @@ def main(argv=None):
                     help="--impl reference: rows of the workload per oracle step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--no-context", action="store_true",
+                    help="skip the L2-hot figure and the torch.topk context figure")
     ap.add_argument("--order", default="workload", choices=["workload", "value", "sample"],
                     help="value: value-ordered output (sorted_index 2; one more launch per call); "
                          "sample: the sampler tail ds_topk_sample (temperature 1, top_p 0.9; "
