@@ -44,6 +44,8 @@ __device__ __forceinline__ float value_at(const void* values, int64_t i) {
 
 template <int ES>
 __global__ void __launch_bounds__(kSampleThreads) topk_sample_kernel(const SampleParams p) {
+  // let the next kernel in the stream be scheduled; wait for the previous one
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the value-ordered selection
   constexpr int kMaxPer = (DS_TOPK_MAX_K + kSampleThreads - 1) / kSampleThreads;
   __shared__ float warp_tot[kSampleThreads / 32];

@@ -1496,16 +1496,31 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
             w[u] = make_uint4(T::kNegInfWord, T::kNegInfWord, T::kNegInfWord, T::kNegInfWord);
             if (v[u] >= 0) w[u] = blk(v[u]);
           }
+          // the UV vectors' counts (above | ties << 16: at most 256 each over the
+          // warp) scanned over the lanes side by side; positions follow list order,
+          // all lanes' vector u before their vector u + 1
+          uint32_t mg[UV], mq[UV], sc[UV];
 #pragma unroll
           for (int u = 0; u < UV; ++u) {
-            uint32_t mg, mq;
-            kstar_masks(w[u], v[u], v[u] >= 0, mg, mq);
-            const uint32_t lg = __popc(mg), lq = __popc(mq);
-            uint32_t bg = base_gt + warp_excl_scan(lg);
-            uint32_t bq = base_eq + warp_excl_scan(lq);
-            base_gt += warp_sum(lg);
-            base_eq += warp_sum(lq);
-            put_masked(w[u], v[u], mg, mq, bg, bq);
+            kstar_masks(w[u], v[u], v[u] >= 0, mg[u], mq[u]);
+            sc[u] = static_cast<uint32_t>(__popc(mg[u])) | (static_cast<uint32_t>(__popc(mq[u])) << 16);
+          }
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+            for (int u = 0; u < UV; ++u) {
+              const uint32_t t = __shfl_up_sync(kFull, sc[u], o);
+              if (lane >= o) sc[u] += t;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < UV; ++u) {
+            const uint32_t tot = __shfl_sync(kFull, sc[u], 31);
+            uint32_t bg = base_gt + (sc[u] & 0xFFFFu) - static_cast<uint32_t>(__popc(mg[u]));
+            uint32_t bq = base_eq + (sc[u] >> 16) - static_cast<uint32_t>(__popc(mq[u]));
+            put_masked(w[u], v[u], mg[u], mq[u], bg, bq);
+            base_gt += tot & 0xFFFFu;
+            base_eq += tot >> 16;
           }
           if (base_gt + min(base_eq, r_ties) >= k) break;
         }

@@ -76,7 +76,8 @@ __device__ __forceinline__ void reg_step(unsigned long long& x0, unsigned long l
 
 template <int ES>
 __global__ void __launch_bounds__(1024) topk_value_order_kernel(const OrderParams p) {
-  // the selection kernel's outputs must be complete before they are read
+  // let the next kernel in the stream be scheduled; wait for the previous one
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ __align__(16) unsigned long long sw[];
   const int tid = threadIdx.x;
@@ -239,6 +240,8 @@ __device__ __forceinline__ void vo_sort_desc(W (&x)[E], int lane) {
 
 template <int E, bool IDX64, bool RETV>
 __global__ void __launch_bounds__(32 * kVoWarps) topk_value_order_warp_kernel(const OrderParams p) {
+  // let the next kernel in the stream be scheduled; wait for the previous one
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the selection's outputs
   constexpr int N = 32 * E;
   __shared__ uint32_t stage[kVoWarps][N + N / 32];
