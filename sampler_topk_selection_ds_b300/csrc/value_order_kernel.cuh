@@ -152,9 +152,6 @@ __global__ void __launch_bounds__(1024) topk_value_order_kernel(const OrderParam
   }
 }
 
-}  // namespace ds_topk_dev
-
-namespace ds_topk_dev {
 
 // ---- one warp per row: bf16 rows of at most 65536 elements, k <= 1024 ----------------
 // A sort word is 32 bits, the 16-bit order key above the complemented 16-bit
