@@ -159,6 +159,16 @@ __device__ __forceinline__ uint32_t key_of(uint32_t bits) {
   }
 }
 
+// Input bits of an order key; -0.0 and +0.0 share a key, so the key of zero
+// returns false and the caller reads the bits back from the input.
+template <int ES>
+__device__ __forceinline__ bool bits_of_key(uint32_t key, uint32_t* bits) {
+  constexpr uint32_t kMid = ES == 2 ? 0x8000u : 0x80000000u;
+  if (key == kMid) return false;
+  *bits = key > kMid ? key - kMid : (kMid | (kMid - key));
+  return true;
+}
+
 template <int ES>
 __device__ __forceinline__ bool is_nan_bits(uint32_t bits) {
   if constexpr (ES == 2) return (bits & 0x7FFFu) > 0x7F80u;
@@ -1230,6 +1240,11 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       // from it but its cost; cluster-uniform
       const bool rd = gv == 1 && G > 1 && misc[kRdMax] > 2u * rd_share + 32u &&
                       rd_share <= static_cast<uint32_t>(rd_cap);
+      // Without spreading, the dead granule-maximum / candidate region keeps each
+      // listed block's masks from the count pass (2 bytes per list entry), so the
+      // write pass reads a block again only for the values it cannot tell from K*.
+      const bool keep_masks = !rd && gv == 1 && union_bytes(p.g_cap_pad, p.cand_cap) >= 2 * static_cast<int64_t>(p.list_cap);
+      uint16_t* vmask = reinterpret_cast<uint16_t*>(uni) + warp * segm;
       uint32_t* ra = reinterpret_cast<uint32_t*>(uni) + warp * rd_cap;  // this warp's share: row vector indices
       int rn = 0;
       if (rd) {
@@ -1411,7 +1426,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
               if (v[u] >= 0) w[u] = blk(v[u]);
             }
 #pragma unroll
-            for (int u = 0; u < UV; ++u) g(w[u], v[u], v[u] >= 0);
+            for (int u = 0; u < UV; ++u) g(w[u], v[u], v[u] >= 0, jb + 32 * u + lane);
           }
           return;
         }
@@ -1419,17 +1434,18 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           for (int j = lane; j < lc; j += 32)
             for (int q = 0; q < gv; ++q) {
               const int64_t v = v0 + static_cast<int64_t>(wlist[j]) * gv + q;
-              if (v < v1) g(blk(v), v, true);
+              if (v < v1) g(blk(v), v, true, j);
             }
         }
       };
       // counts of this warp's list, then prefixes over warps and cluster CTAs
       uint32_t l_gt = 0, l_eq = 0;
-      visit_vecs([&](const uint4& w, int64_t v, bool vok) {
+      visit_vecs([&](const uint4& w, int64_t v, bool vok, int j) {
         uint32_t mg, mq;
         kstar_masks(w, v, vok, mg, mq);
         l_gt += __popc(mg);
         l_eq += __popc(mq);
+        if (keep_masks && vok) vmask[j] = static_cast<uint16_t>(mg | (mq << 8));
       });
       const uint32_t c_gt = warp_sum(l_gt), c_eq = warp_sum(l_eq);
       if (lane == 0) {
@@ -1460,9 +1476,15 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
       // grow from base_gt + min(base_eq, r_ties): when that is already k, this
       // warp has nothing to write.
       const bool none_here = base_gt + min(base_eq, r_ties) >= k;
+      // the value bits of K* itself, unless it is the key of zero (whose sign only
+      // the input holds)
+      uint32_t tie_bits = 0u;
+      const bool tie_known = bits_of_key<ES>(kstar, &tie_bits);
       // writes the elements of masks mg / mq of vector v in index order, from the
-      // lane's running positions bg (above K*) and bq (ties)
-      auto put_masked = [&](const uint4& w, int64_t v, uint32_t mg, uint32_t mq, uint32_t& bg, uint32_t& bq) {
+      // lane's running positions bg (above K*) and bq (ties); values from w, or
+      // (have_w false: ties only, with tie_known) the bits of K*
+      auto put_masked = [&](const uint4& w, bool have_w, int64_t v, uint32_t mg, uint32_t mq, uint32_t& bg,
+                            uint32_t& bq) {
         const int64_t e0 = v * VEC - lead;
         uint32_t m = mg | mq;
         while (m) {
@@ -1478,11 +1500,50 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
           }
           if (pos < k) {
             put_index(p.out_indices, out_base + pos, e0 + e, p.idx64);
-            if (out_val) out_val[pos] = static_cast<VT>(elem_bits<ES>(w, e));
+            if (out_val) out_val[pos] = static_cast<VT>(have_w ? elem_bits<ES>(w, e) : tie_bits);
           }
         }
       };
-      if (gv == 1) {
+      if (gv == 1 && keep_masks) {
+        // the masks kept by the count pass, 8 list entries per lane at a time; a
+        // block is read again only for values above K* (or ties at the key of zero)
+        constexpr int UM = 8;
+        for (int jb = 0; jb < (none_here ? 0 : lcnt); jb += 32 * UM) {
+          uint32_t mg[UM], mq[UM], sc[UM];
+#pragma unroll
+          for (int u = 0; u < UM; ++u) {
+            const int j = jb + 32 * u + lane;
+            const uint32_t m16 = j < lcnt ? vmask[j] : 0u;
+            mg[u] = m16 & 0xFFu;
+            mq[u] = m16 >> 8;
+            sc[u] = static_cast<uint32_t>(__popc(mg[u])) | (static_cast<uint32_t>(__popc(mq[u])) << 16);
+          }
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+            for (int u = 0; u < UM; ++u) {
+              const uint32_t t = __shfl_up_sync(kFull, sc[u], o);
+              if (lane >= o) sc[u] += t;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < UM; ++u) {
+            const uint32_t tot = __shfl_sync(kFull, sc[u], 31);
+            uint32_t bg = base_gt + (sc[u] & 0xFFFFu) - static_cast<uint32_t>(__popc(mg[u]));
+            uint32_t bq = base_eq + (sc[u] >> 16) - static_cast<uint32_t>(__popc(mq[u]));
+            if ((mg[u] | mq[u]) != 0u && bg + min(bq, r_ties) < k) {
+              const int64_t v = vec_at(jb + 32 * u + lane);
+              const bool have_w = out_val != nullptr && (mg[u] != 0u || !tie_known);
+              uint4 w = make_uint4(0u, 0u, 0u, 0u);
+              if (have_w) w = blk(v);
+              put_masked(w, have_w, v, mg[u], mq[u], bg, bq);
+            }
+            base_gt += tot & 0xFFFFu;
+            base_eq += tot >> 16;
+          }
+          if (base_gt + min(base_eq, r_ties) >= k) break;
+        }
+      } else if (gv == 1) {
         // 4 listed vectors in flight per lane, one vector per lane at a time, in
         // list order; stop once every later output would land at or beyond k
         constexpr int UV = 4;
@@ -1518,7 +1579,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
             const uint32_t tot = __shfl_sync(kFull, sc[u], 31);
             uint32_t bg = base_gt + (sc[u] & 0xFFFFu) - static_cast<uint32_t>(__popc(mg[u]));
             uint32_t bq = base_eq + (sc[u] >> 16) - static_cast<uint32_t>(__popc(mq[u]));
-            put_masked(w[u], v[u], mg[u], mq[u], bg, bq);
+            put_masked(w[u], true, v[u], mg[u], mq[u], bg, bq);
             base_gt += tot & 0xFFFFu;
             base_eq += tot >> 16;
           }
@@ -1548,7 +1609,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const Params p) 
                 const uint4 w = blk(vb + q);
                 uint32_t mg, mq;
                 kstar_masks(w, vb + q, true, mg, mq);
-                put_masked(w, vb + q, mg, mq, bg, bq);
+                put_masked(w, true, vb + q, mg, mq, bg, bq);
               }
           }
           if (base_gt + min(base_eq, r_ties) >= k) break;  // warp-uniform

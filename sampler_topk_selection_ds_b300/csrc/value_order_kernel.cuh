@@ -43,16 +43,6 @@ __device__ __forceinline__ uint32_t load_bits(const char* rowp, int64_t i) {
   return *reinterpret_cast<const uint32_t*>(rowp + i * 4);
 }
 
-// Input bits of an order key; -0.0 and +0.0 share a key, so the key of zero
-// returns false and the caller reads the bits back from the input.
-template <int ES>
-__device__ __forceinline__ bool bits_of_key(uint32_t key, uint32_t* bits) {
-  constexpr uint32_t kMid = ES == 2 ? 0x8000u : 0x80000000u;
-  if (key == kMid) return false;
-  *bits = key > kMid ? key - kMid : (kMid | (kMid - key));
-  return true;
-}
-
 // One compare-exchange step of the bitonic network on the two words a lane
 // holds (elements e0 = base + 2 lane and e0 + 1 of its warp's 64-word block).
 __device__ __forceinline__ void reg_step(unsigned long long& x0, unsigned long long& x1, int e0, int size,
