@@ -197,7 +197,9 @@ DS_TOPK_API int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len,
  * A row holding a NaN gets an unspecified but in-range token.
  * Returns DS_TOPK_OK, DS_TOPK_EINVAL (also for a bad temperature or top_p),
  * DS_TOPK_EALIGN or DS_TOPK_ECUDA, like ds_topk; nothing is enqueued on an
- * argument error. Three kernel launches on `stream`; no allocation.
+ * argument error. Kernel launches on `stream`: two when the value order sorts
+ * one row per CTA (that sort draws the tokens too), three after the
+ * one-warp-per-row sort (many bf16 rows); no allocation.
  */
 DS_TOPK_API int ds_topk_sample(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
                    int k, float temperature, float top_p, const float* u, void* out_values,

@@ -462,6 +462,14 @@ cudaError_t launch_dtype(const Plan& pl, cudaStream_t stream) {
 
 bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
 
+// The sampler tail's inputs, for a value-order sort that draws the tokens too.
+struct SampleTail {
+  int32_t* tokens;
+  const float* u;
+  float inv_temperature;
+  float top_p;
+};
+
 // Rows per SM from which the value order sorts one row per warp (measured: with
 // 4 rows per SM the CTA sort is still as fast, from 8 on the warp sort is faster).
 #ifndef DS_TOPK_VO_WARP_ROWS_PER_SM
@@ -493,7 +501,7 @@ cudaError_t launch_vo_warp(cudaLaunchConfig_t cfg, const ds_topk_dev::OrderParam
 template <int ES>
 cudaError_t launch_value_order(const char* x, int64_t batch, int64_t len, int64_t row_stride_bytes, int k,
                                int return_value, void* out_values, void* out_indices, int idx64,
-                               int sm_count, cudaStream_t stream) {
+                               int sm_count, const SampleTail* tail, bool* drawn, cudaStream_t stream) {
   ds_topk_dev::OrderParams op;
   op.x = x;
   op.batch = batch;
@@ -507,6 +515,10 @@ cudaError_t launch_value_order(const char* x, int64_t batch, int64_t len, int64_
   op.out_values = return_value ? out_values : nullptr;
   op.out_indices = out_indices;
   op.idx64 = idx64;
+  op.tokens = nullptr;
+  op.u = nullptr;
+  op.inv_temperature = 1.f;
+  op.top_p = 1.f;
   cudaLaunchConfig_t cfg = {};
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -531,8 +543,16 @@ cudaError_t launch_value_order(const char* x, int64_t batch, int64_t len, int64_
     }
   }
   // The CTA sort is launched plainly: after the cluster selection of the sampler
-  // call it measured 4 us faster without programmatic dependent launch.
+  // call it measured 4 us faster without programmatic dependent launch. It also
+  // draws the sampler tail's tokens when asked to, saving the draw's launch.
   cfg.numAttrs = 0;
+  if (tail) {
+    op.tokens = tail->tokens;
+    op.u = tail->u;
+    op.inv_temperature = tail->inv_temperature;
+    op.top_p = tail->top_p;
+    *drawn = true;
+  }
   const int threads = n2 / 2 < 1024 ? n2 / 2 : 1024;  // n2 >= 64: at least one warp
   const int64_t max_grid = static_cast<int64_t>(sm_count) * 16;
   cfg.gridDim = dim3(static_cast<unsigned>(batch < max_grid ? batch : max_grid), 1, 1);
@@ -544,14 +564,14 @@ cudaError_t launch_value_order(const char* x, int64_t batch, int64_t len, int64_
 // The optional value-order pass after a selection launch; DS_TOPK_OK or DS_TOPK_ECUDA.
 int finish_order(int es, int sorted_index, const void* x, int64_t batch, int64_t len, int64_t row_stride,
                  int k, int return_value, void* out_values, void* out_indices, int idx64, int sm_count,
-                 cudaStream_t stream) {
+                 const SampleTail* tail, bool* drawn, cudaStream_t stream) {
   if (sorted_index != DS_TOPK_SORT_VALUE) return DS_TOPK_OK;
   const char* xb = static_cast<const char*>(x);
   const cudaError_t e =
       es == 2 ? launch_value_order<2>(xb, batch, len, row_stride * 2, k, return_value, out_values, out_indices,
-                                      idx64, sm_count, stream)
+                                      idx64, sm_count, tail, drawn, stream)
               : launch_value_order<4>(xb, batch, len, row_stride * 4, k, return_value, out_values, out_indices,
-                                      idx64, sm_count, stream);
+                                      idx64, sm_count, tail, drawn, stream);
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) {
     cudaGetLastError();
     return DS_TOPK_ECUDA;
@@ -559,11 +579,11 @@ int finish_order(int es, int sorted_index, const void* x, int64_t batch, int64_t
   return DS_TOPK_OK;
 }
 
-}  // namespace
-
-extern "C" int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
-                          int k, int sorted_index, int return_value, int index_type, void* out_values,
-                          void* out_indices, int32_t* nan_flag, cudaStream_t stream) {
+// The TopK call; with a sampler tail (value order only), *drawn tells whether
+// the value-order sort drew the tokens too.
+int topk_impl(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride, int k,
+              int sorted_index, int return_value, int index_type, void* out_values, void* out_indices,
+              int32_t* nan_flag, const SampleTail* tail, bool* drawn, cudaStream_t stream) {
   int rc = validate_sizes(dtype, batch, len, row_stride, k);
   if (rc != DS_TOPK_OK) return rc;
   if (sorted_index < DS_TOPK_SORT_NONE || sorted_index > DS_TOPK_SORT_VALUE ||
@@ -605,7 +625,7 @@ extern "C" int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, 
       return DS_TOPK_ECUDA;
     }
     return finish_order(es, sorted_index, x, batch, len, row_stride, k, return_value, out_values, out_indices,
-                        idx64, dev.sm_count, stream);
+                        idx64, dev.sm_count, tail, drawn, stream);
   }
   int resident = resident_cached(dev_id, pl, dev.sm_count);
   if (resident > 0 && batch > resident) {
@@ -637,7 +657,16 @@ extern "C" int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, 
   }
   if (cudaGetLastError() != cudaSuccess) return DS_TOPK_ECUDA;
   return finish_order(es, sorted_index, x, batch, len, row_stride, k, return_value, out_values, out_indices,
-                      idx64, dev.sm_count, stream);
+                      idx64, dev.sm_count, tail, drawn, stream);
+}
+
+}  // namespace
+
+extern "C" int ds_topk_ex(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride,
+                          int k, int sorted_index, int return_value, int index_type, void* out_values,
+                          void* out_indices, int32_t* nan_flag, cudaStream_t stream) {
+  return topk_impl(x, dtype, batch, len, row_stride, k, sorted_index, return_value, index_type, out_values,
+                   out_indices, nan_flag, nullptr, nullptr, stream);
 }
 
 extern "C" int ds_topk(const void* x, int dtype, int64_t batch, int64_t len, int64_t row_stride, int k,
@@ -658,10 +687,13 @@ extern "C" int ds_topk_sample(const void* x, int dtype, int64_t batch, int64_t l
   if (batch == 0) return DS_TOPK_OK;
   if (!u || !out_tokens || !out_values) return DS_TOPK_EINVAL;
   if (misaligned(u, 4) || misaligned(out_tokens, 4)) return DS_TOPK_EALIGN;
-  // the k survivors in value order, with their values
-  rc = ds_topk(x, dtype, batch, len, row_stride, k, DS_TOPK_SORT_VALUE, 1, out_values, out_indices, nan_flag,
-               stream);
-  if (rc != DS_TOPK_OK) return rc;
+  // the k survivors in value order, with their values (and the draw, when the
+  // value order is one CTA per row)
+  const SampleTail tail{out_tokens, u, 1.0f / temperature, top_p};
+  bool drawn = false;
+  rc = topk_impl(x, dtype, batch, len, row_stride, k, DS_TOPK_SORT_VALUE, 1, DS_TOPK_INDEX_INT32, out_values,
+                 out_indices, nan_flag, &tail, &drawn, stream);
+  if (rc != DS_TOPK_OK || drawn) return rc;
   DeviceInfo dev;
   rc = device_info(&dev);
   if (rc != DS_TOPK_OK) return rc;

@@ -2,7 +2,9 @@
 // k selected logits, the top-p nucleus, and one draw from it.
 //
 // Runs after the value-ordered selection (sorted_index = DS_TOPK_SORT_VALUE with
-// values) on the same stream, one CTA per row. Per row, in fp32:
+// values) on the same stream, one CTA per row, when that value order was the
+// one-warp-per-row sort; the CTA sort draws the same way itself (its draw uses
+// sample_weight below). Per row, in fp32:
 //   w_j = exp((v_j - v_0) / T)   (v_0 the largest value, so w_0 = 1; when v_0 is
 //                                 +inf the +inf values weigh 1 and the rest 0)
 //   C_j = w_0 + ... + w_j        (block-wide inclusive scan)
@@ -42,6 +44,13 @@ __device__ __forceinline__ float value_at(const void* values, int64_t i) {
   return static_cast<const float*>(values)[i];
 }
 
+// Weight of the j-th value-ordered survivor v given the largest v0 (see above).
+__device__ __forceinline__ float sample_weight(float v, float v0, int j, float inv_temperature) {
+  if (isinf(v0) && v0 > 0.f) return v == v0 ? 1.f : 0.f;
+  if (isinf(v0)) return j == 0 ? 1.f : 0.f;  // every value is -inf
+  return expf((v - v0) * inv_temperature);
+}
+
 template <int ES>
 __global__ void __launch_bounds__(kSampleThreads) topk_sample_kernel(const SampleParams p) {
   // let the next kernel in the stream be scheduled; wait for the previous one
@@ -64,12 +73,7 @@ __global__ void __launch_bounds__(kSampleThreads) topk_sample_kernel(const Sampl
     for (int e = 0; e < kMaxPer; ++e) {
       const int j = j0 + e;
       float w = 0.f;
-      if (e < per && j < k) {
-        const float v = value_at<ES>(p.values, base + j);
-        if (isinf(v0) && v0 > 0.f) w = v == v0 ? 1.f : 0.f;
-        else if (isinf(v0)) w = j == 0 ? 1.f : 0.f;  // every value is -inf
-        else w = expf((v - v0) * p.inv_temperature);
-      }
+      if (e < per && j < k) w = sample_weight(value_at<ES>(p.values, base + j), v0, j, p.inv_temperature);
       run += w;
       c[e] = run;  // inclusive within the thread
     }

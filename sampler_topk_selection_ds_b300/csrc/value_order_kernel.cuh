@@ -20,7 +20,7 @@
 // order costs speed, so it is off unless asked for.
 #pragma once
 
-#include "topk_kernel.cuh"
+#include "sampler_kernel.cuh"
 
 namespace ds_topk_dev {
 
@@ -35,7 +35,21 @@ struct OrderParams {
   void* out_values;
   void* out_indices;  // int32 or int64 (idx64)
   int32_t idx64;
+  // sampler tail drawn by the CTA sort right after it (tokens null: none)
+  int32_t* tokens;
+  const float* u;
+  float inv_temperature;
+  float top_p;
 };
+
+// The value of a sort word's order key (the key of zero gives +0: a weight does
+// not see the sign).
+template <int ES>
+__device__ __forceinline__ float word_value(unsigned long long w) {
+  uint32_t bits = 0u;
+  if (!bits_of_key<ES>(static_cast<uint32_t>(w >> 32), &bits)) bits = 0u;
+  return __uint_as_float(ES == 2 ? (bits << 16) : bits);
+}
 
 template <int ES>
 __device__ __forceinline__ uint32_t load_bits(const char* rowp, int64_t i) {
@@ -70,6 +84,9 @@ __global__ void __launch_bounds__(1024) topk_value_order_kernel(const OrderParam
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ __align__(16) unsigned long long sw[];
+  __shared__ float d_warp_tot[32];  // the sampler tail's scratch
+  __shared__ float d_cm;
+  __shared__ int d_m, d_t;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int nt = blockDim.x;  // min(n2 / 2, 1024)
@@ -138,7 +155,71 @@ __global__ void __launch_bounds__(1024) topk_value_order_kernel(const OrderParam
         ov[j] = static_cast<VT>(bits);
       }
     }
-    __syncthreads();  // the next row reuses sw
+    if (p.tokens) {
+      // The sampler tail, on the sorted words still in shared memory: the weights
+      // of the k survivors, their block-wide inclusive scan C, the nucleus end m
+      // (first C_j >= top_p C_{k-1}) and the draw t (first j <= m with C_j > u C_m),
+      // as in topk_sample_kernel, thread tid holding the consecutive j of [j0, j0 + per).
+      constexpr int kMaxPer = 4;  // k <= 4096 over at least k / 4 threads
+      const int per = (p.k + nt - 1) / nt;
+      const int j0 = tid * per;
+      const float v0 = word_value<ES>(sw[0]);
+      float c[kMaxPer];
+      float run = 0.f;
+#pragma unroll
+      for (int e = 0; e < kMaxPer; ++e) {
+        const int j = j0 + e;
+        if (e < per && j < p.k) run += sample_weight(word_value<ES>(sw[j]), v0, j, p.inv_temperature);
+        c[e] = run;
+      }
+      float incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (lane == 31) d_warp_tot[tid >> 5] = incl;
+      if (tid == 0) {
+        d_m = p.k - 1;
+        d_t = 0x7FFFFFFF;
+      }
+      __syncthreads();
+      float before = incl - run, total = 0.f;
+      for (int w = 0; w < nwarps; ++w) {
+        if (w < (tid >> 5)) before += d_warp_tot[w];
+        total += d_warp_tot[w];
+      }
+      const float mass = p.top_p * total;
+#pragma unroll
+      for (int e = 0; e < kMaxPer; ++e) {
+        const int j = j0 + e;
+        if (e < per && j < p.k && before + c[e] >= mass) {
+          atomicMin(&d_m, j);
+          break;
+        }
+      }
+      __syncthreads();
+      const int m = d_m;
+#pragma unroll
+      for (int e = 0; e < kMaxPer; ++e)
+        if (e < per && j0 + e == m) d_cm = before + c[e];
+      __syncthreads();
+      const float target = p.u[row] * d_cm;
+#pragma unroll
+      for (int e = 0; e < kMaxPer; ++e) {
+        const int j = j0 + e;
+        if (e < per && j <= m && before + c[e] > target) {
+          atomicMin(&d_t, j);
+          break;
+        }
+      }
+      __syncthreads();
+      if (tid == 0) {
+        const int t = d_t <= m ? d_t : 0;  // a NaN row finds no step: any in-range choice
+        p.tokens[row] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(sw[t]));
+      }
+    }
+    __syncthreads();  // the next row reuses sw (and the draw's shared words)
   }
 }
 

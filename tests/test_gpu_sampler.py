@@ -93,6 +93,10 @@ def test_sampler_shapes(dtype):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     x = workloads.random_rows(4 * sms + 1, 1000, dtype, 33, style="ties")  # one warp per row
     check_sample(x, 37, 1.3, 0.8, 6)
+    # 8 rows per SM: for bf16 the value order sorts one row per warp and a separate
+    # kernel draws; for fp32 (and above) the CTA sort draws itself
+    x = workloads.random_rows(8 * sms + 3, 1000, dtype, 35, style="normal")
+    check_sample(x, 300, 0.9, 0.95, 8)
 
 
 def test_sampler_degenerate_rows():
