@@ -220,3 +220,32 @@ def test_bench_sample_rows_bounded():
     rows = bench.sample_rows(c4, 256)
     assert len(rows) == 256 and rows[0] == 0 and rows[-1] < c4.batch and rows == sorted(set(rows))
     assert bench.sample_rows(workloads.WORKLOADS["c2"], 256) == list(range(64))
+
+
+@pytest.mark.parametrize("temperature,top_p,u,vals,idx,tok,flag,code", [
+    (0.0, 0.9, P, P, P, P, P, dstk.EINVAL),            # temperature 0
+    (-1.0, 0.9, P, P, P, P, P, dstk.EINVAL),           # negative temperature
+    (float("inf"), 0.9, P, P, P, P, P, dstk.EINVAL),   # infinite temperature
+    (float("nan"), 0.9, P, P, P, P, P, dstk.EINVAL),   # NaN temperature
+    (1.0, 0.0, P, P, P, P, P, dstk.EINVAL),            # top_p 0
+    (1.0, 1.5, P, P, P, P, P, dstk.EINVAL),            # top_p above 1
+    (1.0, float("nan"), P, P, P, P, P, dstk.EINVAL),   # NaN top_p
+    (1.0, 0.9, 0, P, P, P, P, dstk.EINVAL),            # u NULL
+    (1.0, 0.9, P, 0, P, P, P, dstk.EINVAL),            # values NULL (required)
+    (1.0, 0.9, P, P, 0, P, P, dstk.EINVAL),            # indices NULL
+    (1.0, 0.9, P, P, P, 0, P, dstk.EINVAL),            # tokens NULL
+    (1.0, 0.9, P, P, P, P, 0, dstk.EINVAL),            # nan_flag NULL
+    (1.0, 0.9, P + 2, P, P, P, P, dstk.EALIGN),        # u misaligned
+    (1.0, 0.9, P, P, P, P + 2, P, dstk.EALIGN),        # tokens misaligned
+    (1.0, 0.9, P, P + 2, P, P, P, dstk.EALIGN),        # fp32 values misaligned
+])
+def test_sample_argument_errors(temperature, top_p, u, vals, idx, tok, flag, code):
+    """ds_topk_sample validates every argument before it enqueues anything (so
+    these calls need no GPU): the sampling parameters first, then the sizes,
+    pointers and alignments as ds_topk does."""
+    assert dstk.ds_topk_sample(P, dstk.FP32, 4, 4096, 4096, 64, temperature, top_p, u, vals, idx, tok,
+                               flag, 0) == code
+
+
+def test_sample_batch_zero_is_ok_without_pointers():
+    assert dstk.ds_topk_sample(0, dstk.FP32, 0, 4096, 4096, 64, 1.0, 0.9, 0, 0, 0, 0, 0, 0) == dstk.OK
