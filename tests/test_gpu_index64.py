@@ -41,3 +41,21 @@ def test_int64_indices_every_path(dtype, order):
     check_i64(workloads.random_rows(4 * sms + 3, 1000, dtype, 73, style="normal"), 64, order)  # warp rows
     # many rows: for bf16 and value order also the one-warp-per-row sort
     check_i64(workloads.random_rows(8 * sms + 3, 1000, dtype, 74, style="ties"), 300, order)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_int64_indices_value_order_without_values(dtype):
+    """Value order with int64 indices and no values: the sort gathers the keys from
+    x (one warp per row for the bf16 batch of 8 rows per SM, one CTA per row else)."""
+    import sampler_topk_selection_ds_b300 as dstk
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for batch, k in ((8 * sms + 3, 300), (8, 1000)):
+        x = workloads.random_rows(batch, 1000 if batch > 8 else 4096, dtype, 75 + k, style="signed_zero")
+        flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+        _, gi = dstk.topk(x.cuda(), k, sorted_index="value", return_value=False, nan_flag=flag,
+                          index_dtype=torch.int64)
+        torch.cuda.synchronize()
+        _, oi, of, row_nan = oracle.topk(x, k, order="value")
+        assert int(flag.item()) == of and not bool(row_nan.any())
+        assert gi.dtype == torch.int64 and torch.equal(gi.cpu(), oi.to(torch.int64))
+
