@@ -852,8 +852,9 @@ struct WarpRow {
 };
 
 // Margin (in top-16 key units) below the previous row's k-th key for the next
-// row's threshold guess.
-constexpr uint32_t kWrGuessMargin = 6;
+// row's threshold guess. Measured on the decode-shaped call: 8 is fastest (4, 5
+// and 6 cost more failed guesses and their retries, 10 to 16 more candidates).
+constexpr uint32_t kWrGuessMargin = 8;
 
 template <int ES>
 __global__ void __launch_bounds__(kWrThreads, 3) topk_warp_rows_kernel(const WrParams p) {
